@@ -1,0 +1,6 @@
+"""CPU oracle for the Q4_K weight matmul (test infrastructure only).
+
+Imported by the tests, by ``__graft_entry__.smoke()`` and by the CPU
+baseline leg of ``bench.py``; never by the product package.
+"""
+from . import q4k  # noqa: F401

@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of the Q4_K weight matmul on GB300.
+
+Headline: decode GEMV HBM GB/s at batch 1 over the Qwen3-4B-shaped decode
+linear set (q 4096x2560, k/v 1024x2560, o 2560x4096, gate/up 9728x2560,
+down 2560x9728; synthetic Q4_K weights, N(0,1) activations).  One step runs
+the seven GEMVs of one layer; consecutive steps read different copies of the
+layer so that no step finds its weights in L2.
+
+Second leg (same JSON line, key "prefill"): q8_1 quantisation plus the MMQ
+GEMM of the 512-token Qwen3-4B prefill (gate 9728x2560, down 2560x9728).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+GEMV does not shard across GPUs here); value = bytes of all ranks / the
+slowest rank's time.  ``--impl reference`` times the CPU oracle instead, on
+rank 0 only, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "Q4_K GEMV HBM GB/s (batch 1, % of peak); prefill GEMM int8 TOPS & tok/s"
+WORKLOAD = ("Qwen3-4B-shaped decode linear set, batch 1: q 4096x2560, k/v 1024x2560, "
+            "o 2560x4096, gate/up 9728x2560, down 2560x9728 (Q4_K)")
+PREFILL_WORKLOAD = "512-token prefill: q8_1 X[512x2560] x gate 9728x2560, X_down[512x9728] x down 2560x9728"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+BYTES_PER_WEIGHT = 144.0 / 256.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# --------------------------------------------------------------------- peaks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+def profile_traffic(kernel_tag: str, source: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/, valid
+    only while the kernel's source file is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_traffic.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = open(os.path.join(ROOT, "q4_weight_matmul_gb300", "csrc", source), "rb").read()
+    digest = hashlib.sha256(src).hexdigest()[:16]
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != digest:
+        return None
+    return float(m_bytes.group(1))
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        rows = self.rows
+        if self.uuid:
+            mine = [r for r in rows if self.uuid in r[0] or r[0] in self.uuid]
+            rows = mine or rows
+        if not rows:
+            return None
+        uuids = {r[0] for r in rows}
+        if len(uuids) > 1:
+            rows = [r for r in rows if r[0] == sorted(uuids)[0]]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------- oracle (CPU)
+_DECODE_CACHE = {}
+
+
+def decode_inputs():
+    if "layer" not in _DECODE_CACHE:
+        _DECODE_CACHE["layer"] = synth.decode_layer(synth.WL_DECODE_4B, 0, 1)
+    return _DECODE_CACHE["layer"]
+
+
+def oracle_decode_sample(budget_s: float, seed_rows: int = 0):
+    """Time the oracle GEMV on row samples of the seven decode matrices until
+    ``budget_s`` of CPU time is spent.  Returns (GB/s, seconds, description)."""
+    from oracle import q4k as O
+    fields, xs = decode_inputs()
+    rng = np.random.default_rng(seed_rows)
+    done_bytes = 0.0
+    spent = 0.0
+    passes = 0
+    per = 64
+    while spent < budget_s:
+        for name, rows, cols, inp in synth.QWEN3_4B_LAYER:
+            sel = np.sort(rng.choice(rows, per, replace=False))
+            f = {k: v[sel] for k, v in fields[name].items()}
+            t0 = time.perf_counter()
+            O.gemv(f, xs[inp])
+            spent += time.perf_counter() - t0
+            done_bytes += per * cols * BYTES_PER_WEIGHT + cols * 4 + per * 4
+        passes += 1
+    desc = f"oracle GEMV on {passes} passes of {per} random rows of each of the 7 decode matrices"
+    return done_bytes / spent / 1e9, spent, desc
+
+
+def cpu_threads() -> int:
+    try:
+        import threadpoolctl  # noqa: F401
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    # each step: a bounded oracle sample of the decode set (~1 s)
+    vals = []
+    total_bytes = 0.0
+    total_s = 0.0
+    for i in range(args.warmup + args.steps):
+        gbs, spent, desc = oracle_decode_sample(1.0, seed_rows=i)
+        if i >= args.warmup:
+            vals.append(gbs)
+            total_bytes += gbs * spent
+            total_s += spent
+    value = total_bytes / total_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 1, "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world):
+    import torch
+    import q4_weight_matmul_gb300 as q4k
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q4k.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    uuid = str(getattr(props, "uuid", "") or "") or None
+    peaks, peak_kind = measured_peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---------------- weights: pack once, then rotate copies to defeat L2
+    fields, xs_np = decode_inputs()
+    t_pack0 = time.perf_counter()
+    packed = {}
+    pack_bytes = 0
+    pack_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    dev_fields = {}
+    for name, rows, cols, _ in synth.QWEN3_4B_LAYER:
+        f = fields[name]
+        dev_fields[name] = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev)
+                            for k, v in f.items()}
+    torch.cuda.synchronize()
+    pack_ev[0].record()
+    for name, rows, cols, _ in synth.QWEN3_4B_LAYER:
+        d = dev_fields[name]
+        packed[name] = q4k.q4k_pack(d["d"], d["dmin"], d["sc"], d["m"], d["q"])
+        pack_bytes += sum(t.numel() * t.element_size() for t in d.values()) + packed[name].numel()
+    pack_ev[1].record()
+    torch.cuda.synchronize()
+    pack_ms = pack_ev[0].elapsed_time(pack_ev[1])
+    del dev_fields
+    layer_bytes = sum(p.numel() for p in packed.values())
+    n_copies = max(2, math.ceil(4 * l2 / layer_bytes))
+    copies = [packed] + [{k: v.clone() for k, v in packed.items()} for _ in range(n_copies - 1)]
+    xs = {k: torch.from_numpy(v).to(dev) for k, v in xs_np.items()}
+    ys = {name: torch.empty((1, rows), dtype=torch.float32, device=dev)
+          for name, rows, _, _ in synth.QWEN3_4B_LAYER}
+    log(f"[bench] rank {rank}: {n_copies} layer copies x {layer_bytes / 1e6:.1f} MB, pack {pack_ms:.2f} ms "
+        f"(setup {time.perf_counter() - t_pack0:.1f}s)")
+
+    step_bytes = 0.0
+    for name, rows, cols, _ in synth.QWEN3_4B_LAYER:
+        step_bytes += rows * cols * BYTES_PER_WEIGHT + cols * 4 + rows * 4
+
+    n_mat = len(synth.QWEN3_4B_LAYER)
+
+    def decode_step(i, evs=None):
+        layer = copies[i % n_copies]
+        for j, (name, rows, cols, inp) in enumerate(synth.QWEN3_4B_LAYER):
+            if evs is not None:
+                evs[2 * j].record()
+            q4k.q4k_gemv(layer[name], rows, cols, xs[inp], y=ys[name])
+            if evs is not None:
+                evs[2 * j + 1].record()
+
+    for i in range(args.warmup):
+        decode_step(i)
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    launch_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_mat)]
+                  for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    start.record()
+    for i in range(args.steps):
+        decode_step(args.warmup + i, launch_evs[i])
+    stop.record()
+    barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    gemv_ms = sum(ev[2 * j].elapsed_time(ev[2 * j + 1]) for ev in launch_evs for j in range(n_mat))
+    # the same region repeated for long enough to sample clocks under load
+    t_end = time.perf_counter() + 2.0
+    k = 0
+    while time.perf_counter() < t_end:
+        for _ in range(200):
+            decode_step(k)
+            k += 1
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+
+    # ---------------- e2e: public API with host buffers, copies in the region
+    inputs_host = {k: torch.from_numpy(v).pin_memory() for k, v in xs_np.items()}
+    outputs_host = {name: torch.empty((1, rows), dtype=torch.float32).pin_memory()
+                    for name, rows, _, _ in synth.QWEN3_4B_LAYER}
+    h2d = sum(t.numel() * 4 for t in inputs_host.values())
+    d2h = sum(t.numel() * 4 for t in outputs_host.values())
+
+    def e2e_step(i):
+        for k_, t in inputs_host.items():
+            xs[k_].copy_(t, non_blocking=True)
+        decode_step(i)
+        for name, t in outputs_host.items():
+            t.copy_(ys[name], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        e2e_step(args.warmup + i)
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    # ---------------- prefill leg: q8_1 + MMQ GEMM, 512 tokens
+    pf, pxs = synth.prefill_4b_512()
+    pw = {}
+    for name in ("gate", "down"):
+        d = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev)
+             for k, v in pf[name].items()}
+        pw[name] = q4k.q4k_pack(d["d"], d["dmin"], d["sc"], d["m"], d["q"])
+    px = {k: torch.from_numpy(v).to(dev) for k, v in pxs.items()}
+    pbytes = sum(v.numel() for v in pw.values()) + sum(v.numel() * 4 for v in px.values())
+    p_copies = max(2, math.ceil(4 * l2 / pbytes))
+    prefill_sets = [(pw, px)] + [({k: v.clone() for k, v in pw.items()}, {k: v.clone() for k, v in px.items()})
+                                 for _ in range(p_copies - 1)]
+    T = 512
+    pq = {"mlp_in": q4k.q8_quantize(px["mlp_in"]), "down_in": q4k.q8_quantize(px["down_in"])}
+    py = {"gate": torch.empty((T, 9728), device=dev), "down": torch.empty((T, 2560), device=dev)}
+    shapes = {"gate": (9728, 2560, "mlp_in"), "down": (2560, 9728, "down_in")}
+
+    def prefill_step(i, evs=None):
+        wset, xset = prefill_sets[i % p_copies]
+        for j, name in enumerate(("gate", "down")):
+            rows, cols, inp = shapes[name]
+            q, d8, s = pq[inp]
+            q4k.q8_quantize(xset[inp], q, d8, s)
+            if evs is not None:
+                evs[2 * j].record()
+            q4k.q4k_gemm(wset[name], rows, cols, q, d8, s, y=py[name])
+            if evs is not None:
+                evs[2 * j + 1].record()
+
+    for i in range(args.warmup):
+        prefill_step(i)
+    pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record()
+    for i in range(args.steps):
+        prefill_step(args.warmup + i, pevs[i])
+    p1.record()
+    barrier()
+    prefill_ms = p0.elapsed_time(p1)
+    gemm_ms = sum(ev[2 * j].elapsed_time(ev[2 * j + 1]) for ev in pevs for j in range(2))
+    gemm_ops = 2.0 * T * (9728 * 2560 + 2560 * 9728)
+
+    # ---------------- reduce over ranks (max time), sum of work
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    elapsed_ms = max_over_ranks(elapsed_ms)
+    e2e_ms = max_over_ranks(e2e_ms)
+    prefill_ms = max_over_ranks(prefill_ms)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    value = step_bytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    e2e_value = step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9
+    achieved = step_bytes * args.steps / (gemv_ms * 1e-3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    traffic = profile_traffic("gemv_block144", "gemv.cu")
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    gemm_tops = gemm_ops * args.steps / (gemm_ms * 1e-3) / 1e12
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, spent, desc = oracle_decode_sample(args.cpu_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": desc,
+               "seconds": round(spent, 2)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 1, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": f"inputs larger than L2: {n_copies} rotating layer copies "
+                         f"({n_copies * layer_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
+                   "launches_per_step": n_mat},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": f"{peak_kind} hbm_gbs",
+                     "kernel": "gemv_block144_kernel<1>"},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": n_mat * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "pack": {"ms": pack_ms, "GB/s": pack_bytes / (pack_ms * 1e-3) / 1e9, "note": "one-off, 7 matrices"},
+        "prefill": {
+            "workload": PREFILL_WORKLOAD, "tokens": T,
+            "ms_per_step": prefill_ms / args.steps,
+            "tok_s": T * args.steps * world / (prefill_ms * 1e-3),
+            "int_tops": gemm_ops * args.steps * world / (prefill_ms * 1e-3) / 1e12,
+            "gemm_tops": gemm_tops,
+            "roofline": {"bound": "tensor", "achieved": gemm_tops, "unit": "TOPS",
+                         "peak_bf16_dense": bf16, "frac_of_bf16_peak": gemm_tops / bf16},
+            "gpu_launches": 4 * args.steps,
+            "l2": f"{p_copies} rotating weight+input copies",
+        },
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,153 @@
+/*
+ * q4k.h - C ABI of libq4k.so, the GB300 (sm_103a) Q4_K weight-matmul library.
+ *
+ * The library computes the Q4_K-quantised weight matmul of an LLM inference
+ * engine in its two halves (genie-ai-runtime: a Jetson edge LLM inference
+ * engine, §2 "the roofline that dictates strategy"): the bandwidth-bound
+ * decode GEMV and the compute-bound prefill GEMM over q8_1 activations.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All data pointers are DEVICE pointers (cudaMalloc'd or torch-owned) on
+ *    the current CUDA device.  The caller owns every buffer; the library never
+ *    allocates, frees or retains a caller pointer after the call returns.
+ *  - `stream` is a cudaStream_t passed as `void*` (NULL = legacy default
+ *    stream).  Every compute call only validates its arguments on the host
+ *    and enqueues work on `stream`; it returns before the GPU finishes.
+ *  - A non-zero return value is a `q4k_status`; when a call returns anything
+ *    but Q4K_OK nothing was enqueued (Q4K_ERR_CUDA: a launch failed and the
+ *    CUDA error string is available from q4k_last_error_string()).
+ *  - Matrices are row-major.  A weight matrix W has `rows` outputs and `cols`
+ *    inputs; `cols` must be a positive multiple of 256 (one superblock).
+ *    Activations are [tokens][cols], outputs are [tokens][rows].
+ *  - Device pointers must be 16-byte aligned (Q4K_ERR_ALIGNMENT otherwise).
+ *  - Sizes of zero (rows, tokens, batch) are valid and enqueue nothing.
+ *
+ * The Q4_K superblock (genie-ai-runtime §2 "Qwen3-4B Q4_K_M weights"; the
+ * pages name the format but print no byte layout, so the common GGUF Q4_K
+ * byte order is used): 256 weights with an fp16 scale d and an fp16 min
+ * dmin, eight 32-weight sub-blocks with a 6-bit scale sc and a 6-bit min m,
+ * and a 4-bit quant q per weight; each weight is w = d*sc*q - dmin*m.
+ * Q4K_LAYOUT_BLOCK144 stores each superblock in 144 bytes: d (2 bytes,
+ * little-endian binary16), dmin (2), 12 packed scale/min bytes, 128 quant
+ * bytes (weight 64c+l in the low nibble and 64c+32+l in the high nibble of
+ * byte 32c+l).  W occupies rows * (cols/256) * 144 bytes, superblocks of a
+ * row contiguous, rows contiguous.
+ */
+#ifndef Q4K_H
+#define Q4K_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum q4k_status {
+  Q4K_OK = 0,
+  Q4K_ERR_INVALID_ARG = 1,    /* null pointer, bad size or shape           */
+  Q4K_ERR_ALIGNMENT = 2,      /* a pointer is not 16-byte aligned          */
+  Q4K_ERR_UNSUPPORTED = 3,    /* a valid request this build does not serve */
+  Q4K_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed      */
+  Q4K_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up a bounded wait           */
+} q4k_status;
+
+typedef enum q4k_layout {
+  Q4K_LAYOUT_BLOCK144 = 0     /* 144-byte superblocks, GGUF byte order     */
+} q4k_layout;
+
+/* Bytes of a packed rows x cols weight matrix in `layout`
+ * (rows * cols/256 * 144 for BLOCK144); 0 for an invalid request. */
+size_t q4k_packed_bytes(int64_t rows, int64_t cols, int layout);
+
+/*
+ * q4k_pack - pack Q4_K fields into superblocks (the packer/layout step).
+ *   d, dmin : uint16 binary16 bits, [rows][cols/256]
+ *   sc, m   : uint8 values 0..63,   [rows][cols/32]   (bits above 5 ignored)
+ *   q       : uint8 values 0..15,   [rows][cols]      (bits above 3 ignored)
+ *   w       : output, q4k_packed_bytes(rows, cols, layout) bytes
+ * Bit-exact: the result depends only on the input bits.
+ */
+int q4k_pack(const uint16_t* d, const uint16_t* dmin, const uint8_t* sc,
+             const uint8_t* m, const uint8_t* q, int64_t rows, int64_t cols,
+             int layout, void* w, void* stream);
+
+/*
+ * q8_quantize - fp32 activations to q8_1 blocks of 32 (prefill input).
+ * For each row t and each block b of 32 consecutive columns:
+ *   amax = max |x|, d8 = amax / 127 (IEEE fp32 division),
+ *   q = clamp(roundf(x / d8), -127, 127) (fp32 division, ties away from 0),
+ *   sum = sum of the 32 q; a block whose d8 is 0 gives q = 0, sum = 0.
+ *   x   : float [tokens][cols]   (cols a multiple of 256)
+ *   q   : int8  [tokens][cols]
+ *   d8  : float [tokens][cols/32]
+ *   sum : int32 [tokens][cols/32]
+ * Bit-exact.  Non-finite inputs give unspecified (but in-bounds) output.
+ */
+int q8_quantize(const float* x, int64_t tokens, int64_t cols, int8_t* q,
+                float* d8, int32_t* sum, void* stream);
+
+/*
+ * q4k_gemv - decode GEMV (genie-ai-runtime §4, Path C: the hot decode
+ * kernels; residual add folded into the GEMV):
+ *   y[b][o] = sum_k w[o][k] * x[b][k]  (+ residual[b][o] if residual != NULL)
+ *   w        : packed weights (layout), rows x cols
+ *   x        : float [batch][cols], 1 <= batch <= 8
+ *   residual : float [batch][rows] or NULL
+ *   y        : float [batch][rows]; may alias residual, not x or w
+ * Accuracy: |y - exact| <= 1e-4 * sum_k |w||x| (+|residual|) per element.
+ * Deterministic: the same inputs give the same bits on every run.
+ */
+int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols,
+             const float* x, int64_t batch, const float* residual, float* y,
+             void* stream);
+
+/*
+ * q4k_gemm - prefill MMQ GEMM (genie-ai-runtime §3, "The tensor-core kernel
+ * (Path E)"; integer form over q8_1 activations):
+ *   y[t][o] = sum_b ( d*sc[o,b] * d8[t,b] * P[t,o,b]
+ *                     - dmin*m[o,b] * d8[t,b] * sum[t,b] ),
+ *   P[t,o,b] = sum_{i<32} q[o][32b+i] * q8[t][32b+i]   (exact integers)
+ *   w         : packed weights (layout), rows x cols
+ *   q8,d8,sum : q8_quantize() output for `tokens` rows of width cols
+ *   y         : float [tokens][rows]
+ * Accuracy: |y - exact| <= 1e-4 * sum_k |w| |d8 q8| per element.
+ */
+int q4k_gemm(const void* w, int layout, int64_t rows, int64_t cols,
+             const int8_t* q8, const float* d8, const int32_t* sum,
+             int64_t tokens, float* y, void* stream);
+
+/*
+ * q4k_gemm_blockdots - test export of the GEMM's per-block integer dots,
+ * computed by the same tensor-core main loop as q4k_gemm:
+ *   p[t][o][b] = sum_{i<32} q[o][32b+i] * q8[t][32b+i]
+ *   p : int32 [tokens][rows][cols/32]
+ * Bit-exact.
+ */
+int q4k_gemm_blockdots(const void* w, int layout, int64_t rows, int64_t cols,
+                       const int8_t* q8, int64_t tokens, int32_t* p,
+                       void* stream);
+
+/*
+ * q4k_device_error - synchronise `stream` and read (then clear) the
+ * library's device-side error word on the current device.  Returns Q4K_OK,
+ * Q4K_ERR_DEVICE_TIMEOUT if a kernel abandoned a bounded wait since the last
+ * read, or Q4K_ERR_CUDA if the synchronisation itself failed.
+ */
+int q4k_device_error(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* q4k_status_string(int status);
+
+/* Thread-local text of the last CUDA error seen by a call ("" if none). */
+const char* q4k_last_error_string(void);
+
+/* Library version, e.g. "q4k 0.1.0 sm_103a". */
+const char* q4k_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4K_H */

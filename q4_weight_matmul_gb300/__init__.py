@@ -1,0 +1,178 @@
+"""Python binding of libq4k.so, the GB300 Q4_K weight-matmul library.
+
+Argument marshalling only: every function checks that its torch tensors are
+contiguous CUDA tensors of the expected dtype, passes their device pointers
+and the current torch stream to the C ABI (``include/q4k.h``) and raises
+``Q4KError`` on a non-OK status.  All arithmetic runs in the library's CUDA
+kernels; there is no CPU path.  Importing works without a GPU (the library
+loads), but every compute call needs the CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH, build
+
+BLOCK144 = 0
+Q4K_OK = 0
+QK_K = 256
+QK_SUB = 32
+
+_STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_INVALID_ARG", 2: "Q4K_ERR_ALIGNMENT",
+           3: "Q4K_ERR_UNSUPPORTED", 4: "Q4K_ERR_CUDA", 5: "Q4K_ERR_DEVICE_TIMEOUT"}
+
+# Every symbol the header declares, with its ctypes signature.
+_P, _I64, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+SIGNATURES = {
+    "q4k_packed_bytes": (ctypes.c_size_t, [_I64, _I64, _I]),
+    "q4k_pack": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _P, _P]),
+    "q8_quantize": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "q4k_gemv": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "q4k_gemm": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
+    "q4k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
+    "q4k_device_error": (_I, [_P]),
+    "q4k_status_string": (ctypes.c_char_p, [_I]),
+    "q4k_last_error_string": (ctypes.c_char_p, []),
+    "q4k_version": (ctypes.c_char_p, []),
+}
+
+
+class Q4KError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        detail = ""
+        if status == 4 and _lib is not None:
+            detail = ": " + _lib.q4k_last_error_string().decode()
+        super().__init__(f"{call} failed with {_STATUS.get(status, status)}{detail}")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libq4k.so (built in-tree by ``build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run q4_weight_matmul_gb300.build.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t, dtype, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _ptr16(t, name):
+    """binary16 bit patterns may arrive as uint16, int16 or float16 tensors."""
+    kinds = (torch.int16, torch.float16) + ((torch.uint16,) if hasattr(torch, "uint16") else ())
+    if not isinstance(t, torch.Tensor) or t.dtype not in kinds:
+        raise TypeError(f"{name} must hold binary16 bits (uint16/int16/float16)")
+    return _ptr(t, t.dtype, name)
+
+
+def _check(status: int, call: str):
+    if status != Q4K_OK:
+        raise Q4KError(status, call)
+
+
+def q4k_packed_bytes(rows: int, cols: int, layout: int = BLOCK144) -> int:
+    return int(lib().q4k_packed_bytes(rows, cols, layout))
+
+
+def q4k_pack(d, dmin, sc, m, q, out=None, layout: int = BLOCK144, stream=None):
+    """Pack Q4_K fields (uint16 d/dmin bits, uint8 sc/m/q) into ``out``
+    (uint8, ``q4k_packed_bytes`` long; allocated when None)."""
+    rows, cols = q.shape
+    if out is None:
+        out = torch.empty(q4k_packed_bytes(rows, cols, layout), dtype=torch.uint8, device=q.device)
+    _check(lib().q4k_pack(_ptr16(d, "d"), _ptr16(dmin, "dmin"),
+                          _ptr(sc, torch.uint8, "sc"), _ptr(m, torch.uint8, "m"),
+                          _ptr(q, torch.uint8, "q"), rows, cols, layout,
+                          _ptr(out, torch.uint8, "out"), _stream(stream)), "q4k_pack")
+    return out
+
+
+def q8_quantize(x, q=None, d8=None, s=None, stream=None):
+    """q8_1-quantise ``x`` [tokens][cols] float32; returns (q int8, d8 float32, sum int32)."""
+    tokens, cols = x.shape
+    dev = x.device
+    q = torch.empty((tokens, cols), dtype=torch.int8, device=dev) if q is None else q
+    d8 = torch.empty((tokens, cols // QK_SUB), dtype=torch.float32, device=dev) if d8 is None else d8
+    s = torch.empty((tokens, cols // QK_SUB), dtype=torch.int32, device=dev) if s is None else s
+    _check(lib().q8_quantize(_ptr(x, torch.float32, "x"), tokens, cols, _ptr(q, torch.int8, "q"),
+                             _ptr(d8, torch.float32, "d8"), _ptr(s, torch.int32, "sum"),
+                             _stream(stream)), "q8_quantize")
+    return q, d8, s
+
+
+def q4k_gemv(w, rows: int, cols: int, x, residual=None, y=None, layout: int = BLOCK144, stream=None):
+    """Decode GEMV: ``y[b] = W x[b] (+ residual[b])`` for ``x`` [batch][cols] float32."""
+    batch = x.shape[0]
+    if y is None:
+        y = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    _check(lib().q4k_gemv(_ptr(w, torch.uint8, "w"), layout, rows, cols,
+                          _ptr(x, torch.float32, "x"), batch,
+                          _ptr(residual, torch.float32, "residual"),
+                          _ptr(y, torch.float32, "y"), _stream(stream)), "q4k_gemv")
+    return y
+
+
+def q4k_gemm(w, rows: int, cols: int, q8, d8, s, y=None, layout: int = BLOCK144, stream=None):
+    """Prefill MMQ GEMM on q8_1 activations; returns ``y`` [tokens][rows] float32."""
+    tokens = q8.shape[0]
+    if y is None:
+        y = torch.empty((tokens, rows), dtype=torch.float32, device=q8.device)
+    _check(lib().q4k_gemm(_ptr(w, torch.uint8, "w"), layout, rows, cols,
+                          _ptr(q8, torch.int8, "q8"), _ptr(d8, torch.float32, "d8"),
+                          _ptr(s, torch.int32, "sum"), tokens, _ptr(y, torch.float32, "y"),
+                          _stream(stream)), "q4k_gemm")
+    return y
+
+
+def q4k_gemm_blockdots(w, rows: int, cols: int, q8, p=None, layout: int = BLOCK144, stream=None):
+    """Test export: the GEMM's exact per-block integer dots, int32 [tokens][rows][cols/32]."""
+    tokens = q8.shape[0]
+    if p is None:
+        p = torch.empty((tokens, rows, cols // QK_SUB), dtype=torch.int32, device=q8.device)
+    _check(lib().q4k_gemm_blockdots(_ptr(w, torch.uint8, "w"), layout, rows, cols,
+                                    _ptr(q8, torch.int8, "q8"), tokens,
+                                    _ptr(p, torch.int32, "p"), _stream(stream)),
+           "q4k_gemm_blockdots")
+    return p
+
+
+def q4k_device_error(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device error status."""
+    return int(lib().q4k_device_error(_stream(stream)))
+
+
+def q4k_version() -> str:
+    return lib().q4k_version().decode()
+
+
+__all__ = ["build", "lib", "Q4KError", "BLOCK144", "q4k_packed_bytes", "q4k_pack", "q8_quantize",
+           "q4k_gemv", "q4k_gemm", "q4k_gemm_blockdots", "q4k_device_error", "q4k_version",
+           "SIGNATURES"]

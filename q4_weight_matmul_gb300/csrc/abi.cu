@@ -1,0 +1,192 @@
+// The C ABI of libq4k.so (declared in include/q4k.h): host-side argument
+// validation, then one asynchronous launch on the caller's stream.  Nothing
+// here allocates device memory; the only device state the library owns is a
+// per-device error word that kernels with bounded waits set when they give up.
+#include "q4k_internal.h"
+
+#include <q4k.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+namespace q4k {
+
+__device__ int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ready[kMaxDevices];
+int* g_error_ptr[kMaxDevices];
+thread_local char g_last_error[256] = "";
+
+int record_cuda(cudaError_t e) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return Q4K_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_cols(int64_t cols) {
+  if (cols <= 0 || cols % kQK != 0 || cols > (int64_t(1) << 24)) return Q4K_ERR_INVALID_ARG;
+  return Q4K_OK;
+}
+
+int check_layout(int layout) {
+  return layout == Q4K_LAYOUT_BLOCK144 ? Q4K_OK : Q4K_ERR_UNSUPPORTED;
+}
+
+int check_rows(int64_t rows) {
+  return (rows < 0 || rows > (int64_t(1) << 24)) ? Q4K_ERR_INVALID_ARG : Q4K_OK;
+}
+
+}  // namespace
+
+const DeviceInfo& device_info(int device) {
+  if (device < 0 || device >= kMaxDevices) device = 0;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_info_ready[device]) {
+    DeviceInfo& d = g_info[device];
+    cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
+    cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, device);
+    if (d.sm_count <= 0) d.sm_count = 1;
+    g_info_ready[device] = true;
+  }
+  return g_info[device];
+}
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_error_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_error_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_error_ptr[dev];
+}
+
+}  // namespace q4k
+
+using namespace q4k;
+
+extern "C" {
+
+size_t q4k_packed_bytes(int64_t rows, int64_t cols, int layout) {
+  if (check_rows(rows) || check_cols(cols) || check_layout(layout)) return 0;
+  return (size_t)rows * (size_t)(cols / kQK) * kBlockBytes;
+}
+
+int q4k_pack(const uint16_t* d, const uint16_t* dmin, const uint8_t* sc,
+             const uint8_t* m, const uint8_t* q, int64_t rows, int64_t cols,
+             int layout, void* w, void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_layout(layout)) return e;
+  if (rows == 0) return Q4K_OK;
+  if (!d || !dmin || !sc || !m || !q || !w) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(d) || !aligned16(dmin) || !aligned16(sc) || !aligned16(m) || !aligned16(q) ||
+      !aligned16(w))
+    return Q4K_ERR_ALIGNMENT;
+  cudaError_t e = launch_pack_block144(d, dmin, sc, m, q, rows, cols, static_cast<uint8_t*>(w),
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+int q8_quantize(const float* x, int64_t tokens, int64_t cols, int8_t* q, float* d8,
+                int32_t* sum, void* stream) {
+  if (tokens < 0 || tokens > (int64_t(1) << 24)) return Q4K_ERR_INVALID_ARG;
+  if (int e = check_cols(cols)) return e;
+  if (tokens == 0) return Q4K_OK;
+  if (!x || !q || !d8 || !sum) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(d8) || !aligned16(sum)) return Q4K_ERR_ALIGNMENT;
+  cudaError_t e = launch_q8_quantize(x, tokens, cols, q, d8, sum, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols, const float* x,
+             int64_t batch, const float* residual, float* y, void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_layout(layout)) return e;
+  if (batch < 0 || batch > 8) return batch < 0 ? Q4K_ERR_INVALID_ARG : Q4K_ERR_UNSUPPORTED;
+  if (rows == 0 || batch == 0) return Q4K_OK;
+  if (!w || !x || !y) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)))
+    return Q4K_ERR_ALIGNMENT;
+  if (!gemv_supported(cols, (int)batch)) return Q4K_ERR_UNSUPPORTED;
+  cudaError_t e = launch_gemv_block144(static_cast<const uint8_t*>(w), rows, cols, x, (int)batch,
+                                       residual, y, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return Q4K_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+static int gemm_common(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8,
+                       const float* d8, const int32_t* sum, int64_t tokens, float* y,
+                       int32_t* p, void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_layout(layout)) return e;
+  if (tokens < 0 || tokens > (int64_t(1) << 22)) return Q4K_ERR_INVALID_ARG;
+  if (rows == 0 || tokens == 0) return Q4K_OK;
+  if (!w || !q8) return Q4K_ERR_INVALID_ARG;
+  if (!p && (!d8 || !sum || !y)) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(q8) || (d8 && !aligned16(d8)) || (sum && !aligned16(sum)) ||
+      (y && !aligned16(y)) || (p && !aligned16(p)))
+    return Q4K_ERR_ALIGNMENT;
+  cudaError_t e = launch_gemm_dp4a(static_cast<const uint8_t*>(w), rows, cols, q8, d8, sum, tokens,
+                                   y, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+int q4k_gemm(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8,
+             const float* d8, const int32_t* sum, int64_t tokens, float* y, void* stream) {
+  return gemm_common(w, layout, rows, cols, q8, d8, sum, tokens, y, nullptr, stream);
+}
+
+int q4k_gemm_blockdots(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8,
+                       int64_t tokens, int32_t* p, void* stream) {
+  if (!p && rows != 0 && tokens != 0) return Q4K_ERR_INVALID_ARG;
+  return gemm_common(w, layout, rows, cols, q8, nullptr, nullptr, tokens, nullptr, p, stream);
+}
+
+int q4k_device_error(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e);
+  int* word = device_error_word();
+  if (!word) return record_cuda(cudaGetLastError());
+  int value = 0;
+  e = cudaMemcpy(&value, word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return record_cuda(e);
+  if (value != 0) {
+    const int zero = 0;
+    e = cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return record_cuda(e);
+    return Q4K_ERR_DEVICE_TIMEOUT;
+  }
+  return Q4K_OK;
+}
+
+const char* q4k_status_string(int status) {
+  switch (status) {
+    case Q4K_OK: return "Q4K_OK";
+    case Q4K_ERR_INVALID_ARG: return "Q4K_ERR_INVALID_ARG";
+    case Q4K_ERR_ALIGNMENT: return "Q4K_ERR_ALIGNMENT";
+    case Q4K_ERR_UNSUPPORTED: return "Q4K_ERR_UNSUPPORTED";
+    case Q4K_ERR_CUDA: return "Q4K_ERR_CUDA";
+    case Q4K_ERR_DEVICE_TIMEOUT: return "Q4K_ERR_DEVICE_TIMEOUT";
+    default: return "Q4K_ERR_UNKNOWN";
+  }
+}
+
+const char* q4k_last_error_string(void) { return g_last_error; }
+
+const char* q4k_version(void) { return "q4k 0.1.0 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,57 @@
+// Internal declarations shared by the library's translation units.
+// Launchers validate nothing: the C-ABI layer (abi.cu) checks every argument
+// before it calls one.  Each returns the cudaError_t of its launch.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace q4k {
+
+constexpr int kQK = 256;         // weights per superblock
+constexpr int kSub = 32;         // weights per sub-block
+constexpr int kBlockBytes = 144; // bytes of one BLOCK144 superblock
+
+// Device properties the launchers size their grids by (cached per device).
+struct DeviceInfo {
+  int sm_count;
+  int max_smem_optin;   // bytes of dynamic shared memory a CTA may opt into
+  int l2_bytes;
+};
+const DeviceInfo& device_info(int device);
+
+// Library-owned device error word of the current device (see abi.cu).
+int* device_error_word();
+
+cudaError_t launch_pack_block144(const uint16_t* d, const uint16_t* dmin,
+                                 const uint8_t* sc, const uint8_t* m,
+                                 const uint8_t* q, int64_t rows, int64_t cols,
+                                 uint8_t* w, cudaStream_t s);
+
+cudaError_t launch_q8_quantize(const float* x, int64_t tokens, int64_t cols,
+                               int8_t* q, float* d8, int32_t* sum,
+                               cudaStream_t s);
+
+// Returns cudaErrorNotSupported when (batch, cols) does not fit the kernel's
+// shared-memory staging of the activations.
+cudaError_t launch_gemv_block144(const uint8_t* w, int64_t rows, int64_t cols,
+                                 const float* x, int batch,
+                                 const float* residual, float* y,
+                                 cudaStream_t s);
+bool gemv_supported(int64_t cols, int batch);
+
+// Small-tile integer MMQ on CUDA cores (dp4a).  When `p_out` is non-null
+// the kernel stores the raw per-block integer dots there instead of y.
+cudaError_t launch_gemm_dp4a(const uint8_t* w, int64_t rows, int64_t cols,
+                             const int8_t* q8, const float* d8,
+                             const int32_t* sum, int64_t tokens, float* y,
+                             int32_t* p_out, cudaStream_t s);
+
+// Prefill MMQ GEMM.  When `p_out` is non-null the kernel stores the raw
+// per-block integer dots there instead of y (test export).
+cudaError_t launch_gemm_block144(const uint8_t* w, int64_t rows, int64_t cols,
+                                 const int8_t* q8, const float* d8,
+                                 const int32_t* sum, int64_t tokens, float* y,
+                                 int32_t* p_out, int* err, cudaStream_t s);
+
+}  // namespace q4k

@@ -1,0 +1,74 @@
+"""Run one library kernel on a small synthetic case, for profiler captures.
+
+    python -m q4_weight_matmul_gb300.profile_case gemv --rows 9728 --cols 2560 --batch 1 --reps 5
+    python -m q4_weight_matmul_gb300.profile_case gemm --rows 9728 --cols 2560 --tokens 512
+    python -m q4_weight_matmul_gb300.profile_case q8 --tokens 512 --cols 9728
+    python -m q4_weight_matmul_gb300.profile_case pack --rows 9728 --cols 2560
+
+Inputs are uniformly random bytes / N(0,1) floats (valid Q4_K fields), made on
+the device; nothing is checked here (the tests do that).  Weights are spread
+over enough copies that consecutive launches miss L2.
+"""
+from __future__ import annotations
+
+import argparse
+import math
+
+import torch
+
+import q4_weight_matmul_gb300 as q4k
+
+
+def rand_fields(rows, cols, dev, gen):
+    nb = cols // 256
+    d = (torch.rand((rows, nb), generator=gen, device=dev) * 0.02).half().view(torch.int16)
+    dmin = (torch.rand((rows, nb), generator=gen, device=dev) * 0.02).half().view(torch.int16)
+    sc = torch.randint(0, 64, (rows, cols // 32), generator=gen, device=dev, dtype=torch.uint8)
+    m = torch.randint(0, 64, (rows, cols // 32), generator=gen, device=dev, dtype=torch.uint8)
+    q = torch.randint(0, 16, (rows, cols), generator=gen, device=dev, dtype=torch.uint8)
+    return d, dmin, sc, m, q
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("kernel", choices=["gemv", "gemm", "q8", "pack"])
+    ap.add_argument("--rows", type=int, default=9728)
+    ap.add_argument("--cols", type=int, default=2560)
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--tokens", type=int, default=512)
+    ap.add_argument("--reps", type=int, default=5)
+    a = ap.parse_args()
+    q4k.build()
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
+    f = rand_fields(a.rows, a.cols, dev, gen)
+    w0 = q4k.q4k_pack(*f)
+    n = max(1, math.ceil(2 * l2 / w0.numel())) if a.kernel in ("gemv", "gemm") else 1
+    ws = [w0] + [w0.clone() for _ in range(n - 1)]
+    if a.kernel == "gemv":
+        x = torch.randn((a.batch, a.cols), device=dev, generator=gen)
+        y = torch.empty((a.batch, a.rows), device=dev)
+        for i in range(a.reps):
+            q4k.q4k_gemv(ws[i % n], a.rows, a.cols, x, y=y)
+    elif a.kernel == "gemm":
+        x = torch.randn((a.tokens, a.cols), device=dev, generator=gen)
+        q, d8, s = q4k.q8_quantize(x)
+        y = torch.empty((a.tokens, a.rows), device=dev)
+        for i in range(a.reps):
+            q4k.q4k_gemm(ws[i % n], a.rows, a.cols, q, d8, s, y=y)
+    elif a.kernel == "q8":
+        x = torch.randn((a.tokens, a.cols), device=dev, generator=gen)
+        out = q4k.q8_quantize(x)
+        for _ in range(a.reps):
+            q4k.q8_quantize(x, *out)
+    else:
+        for _ in range(a.reps):
+            q4k.q4k_pack(*f, out=w0)
+    torch.cuda.synchronize()
+    print("profile case done:", a.kernel, a.rows, a.cols, a.batch, a.tokens, a.reps)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,94 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument validation returns the documented status codes (no GPU needed: no
+call here reaches a CUDA launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q4k.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from q4_weight_matmul_gb300.build import build
+    path = build()
+    handle = ctypes.CDLL(path)
+    import q4_weight_matmul_gb300 as q4k
+    for name, (res, args) in q4k.SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype, fn.argtypes = res, args
+    return handle
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return sorted(set(re.findall(r"\b((?:q4k|q8)_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("q4k_pack", "q8_quantize", "q4k_gemv", "q4k_gemm"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import q4_weight_matmul_gb300 as q4k
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in q4k.SIGNATURES, f"binding lacks {name}"
+
+
+def test_packed_bytes(lib):
+    assert lib.q4k_packed_bytes(9728, 2560, 0) == 9728 * 10 * 144
+    assert lib.q4k_packed_bytes(1, 256, 0) == 144
+    assert lib.q4k_packed_bytes(0, 256, 0) == 0
+    assert lib.q4k_packed_bytes(4, 100, 0) == 0        # cols not a multiple of 256
+    assert lib.q4k_packed_bytes(4, 256, 7) == 0        # unknown layout
+    assert lib.q4k_packed_bytes(-1, 256, 0) == 0
+
+
+def test_status_strings_and_version(lib):
+    assert lib.q4k_status_string(0) == b"Q4K_OK"
+    assert lib.q4k_status_string(5) == b"Q4K_ERR_DEVICE_TIMEOUT"
+    assert lib.q4k_status_string(99) == b"Q4K_ERR_UNKNOWN"
+    assert b"sm_103a" in lib.q4k_version()
+
+
+def test_validation_before_any_launch(lib):
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(0x10008)
+    # cols must be a positive multiple of 256
+    assert lib.q4k_gemv(fake, 0, 8, 300, fake, 1, None, fake, None) == 1
+    assert lib.q4k_gemm(fake, 0, 8, 0, fake, fake, fake, 4, fake, None) == 1
+    assert lib.q8_quantize(fake, 2, 100, fake, fake, fake, None) == 1
+    # unknown layout
+    assert lib.q4k_gemv(fake, 9, 8, 256, fake, 1, None, fake, None) == 3
+    # batch out of range
+    assert lib.q4k_gemv(fake, 0, 8, 256, fake, 9, None, fake, None) == 3
+    assert lib.q4k_gemv(fake, 0, 8, 256, fake, -1, None, fake, None) == 1
+    # null pointers
+    assert lib.q4k_gemv(None, 0, 8, 256, fake, 1, None, fake, None) == 1
+    assert lib.q4k_gemm(fake, 0, 8, 256, fake, None, fake, 4, fake, None) == 1
+    assert lib.q4k_pack(fake, fake, fake, None, fake, 2, 256, 0, fake, None) == 1
+    # misaligned pointers
+    assert lib.q4k_pack(fake, fake, fake, fake, odd, 2, 256, 0, fake, None) == 2
+    assert lib.q8_quantize(odd, 2, 256, fake, fake, fake, None) == 2
+    assert lib.q4k_gemm(fake, 0, 8, 256, fake, fake, fake, 4, odd, None) == 2
+    # empty problems enqueue nothing and succeed
+    assert lib.q4k_gemv(None, 0, 0, 256, None, 1, None, None, None) == 0
+    assert lib.q4k_gemm(None, 0, 8, 256, None, None, None, 0, None, None) == 0
+    assert lib.q8_quantize(None, 0, 256, None, None, None, None) == 0
+    assert lib.q4k_pack(None, None, None, None, None, 0, 256, 0, None, None) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import q4_weight_matmul_gb300 as q4k
+    x = torch.zeros(1, 256)
+    with pytest.raises(TypeError):
+        q4k.q8_quantize(x)

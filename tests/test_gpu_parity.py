@@ -1,0 +1,183 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Integer stages are compared bit for bit; fp outputs must
+satisfy |y - y_ref| <= 1e-4 * sum|w||x| element by element."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import q4k as O
+import synth
+from _gpu import pack_dev, slice_rows, to_dev
+import q4_weight_matmul_gb300 as q4k
+
+pytestmark = pytest.mark.gpu
+REL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    q4k.build()
+    torch.cuda.init()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def assert_close(y, y_ref, norm, what=""):
+    ok, worst = O.within_tolerance(y, y_ref, norm, REL)
+    assert ok, f"{what}: worst error {worst:.3g} x the allowed 1e-4*sum|w||x|"
+
+
+# ------------------------------------------------------------------ pack
+@pytest.mark.parametrize("rows,cols", [(1, 256), (3, 768), (17, 2560), (64, 4096), (9728, 2560),
+                                       (2560, 9728)])
+def test_pack_bit_exact(rows, cols):
+    f = synth.q4k_fields(rows, cols, [rows, cols])
+    got = host(pack_dev(f)).reshape(rows, cols // 256, 144)
+    assert np.array_equal(got, O.pack_block144(f))
+
+
+def test_pack_ignores_bits_above_each_field():
+    f = synth.q4k_fields(5, 512, 77)
+    junk = dict(f)
+    junk["sc"] = f["sc"] | 0xC0
+    junk["m"] = f["m"] | 0x40
+    junk["q"] = f["q"] | 0xF0
+    assert np.array_equal(host(pack_dev(junk)), host(pack_dev(f)))
+
+
+# ------------------------------------------------------------------ q8_1
+def adversarial_activations():
+    x = synth.activations(8, 512, 55)
+    x[0, :32] = 0.0                                  # zero block
+    x[1, :32] = np.arange(-16, 16) * 0.5             # exact ties after scaling
+    x[1, 0] = -127 * 0.125
+    x[2, :32] = 1e-44                                # d8 underflows to zero
+    x[3, :32] = np.float32(3e38) * np.sign(np.arange(32) - 15.5)
+    x[4, :32] = 2.5                                  # all equal
+    x[5, 32:64] = -x[5, 32:64]
+    x[6, :] *= np.float32(1e-30)
+    return x
+
+
+@pytest.mark.parametrize("case", ["adversarial", (1, 256), (5, 768), (512, 2560), (512, 9728)])
+def test_q8_quantize_bit_exact(case):
+    x = adversarial_activations() if case == "adversarial" else synth.activations(*case, 300)
+    q, d8, s = q4k.q8_quantize(torch.from_numpy(x).cuda())
+    rq, rd, rs = O.quantize_q8_1(x)
+    assert np.array_equal(host(q), rq)
+    assert np.array_equal(host(d8).view(np.uint32), rd.view(np.uint32))
+    assert np.array_equal(host(s), rs)
+
+
+# ------------------------------------------------------------------ GEMV
+def run_gemv(f, x, r=None, w=None):
+    rows, cols = f["q"].shape
+    w = pack_dev(f) if w is None else w
+    xd = torch.from_numpy(x).cuda()
+    rd = None if r is None else torch.from_numpy(r).cuda()
+    return host(q4k.q4k_gemv(w, rows, cols, xd, residual=rd))
+
+
+@pytest.mark.parametrize("rows,cols,batch,res", [
+    (1, 256, 1, False), (7, 768, 1, True), (8, 512, 2, False), (33, 2560, 1, False),
+    (100, 1024, 3, True), (513, 4096, 4, False), (1024, 9728, 1, True), (257, 2560, 8, False),
+    (3000, 256, 1, False)])
+def test_gemv_parity(rows, cols, batch, res):
+    f = synth.q4k_fields(rows, cols, [rows, cols, batch])
+    x = synth.activations(batch, cols, [batch, cols])
+    r = synth.residual(batch, rows, [7, rows]) if res else None
+    y = run_gemv(f, x, r)
+    y_ref, norm = O.gemv(f, x, r)
+    assert_close(y, y_ref, norm, f"gemv {rows}x{cols} b{batch}")
+
+
+def test_gemv_single_2048_seed0():
+    f, x = synth.single_gemv_2048(0)
+    y = run_gemv(f, x)
+    y_ref, norm = O.gemv(f, x)
+    assert_close(y, y_ref, norm, "2048x2048")
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_gemv_qwen3_4b_decode_set(batch):
+    fields, xs = synth.decode_layer(synth.WL_DECODE_4B, 0, batch)
+    for name, rows, cols, inp in synth.QWEN3_4B_LAYER:
+        y = run_gemv(fields[name], xs[inp])
+        y_ref, norm = O.gemv(fields[name], xs[inp])
+        assert_close(y, y_ref, norm, name)
+
+
+def test_gemv_is_deterministic():
+    f = synth.q4k_fields(2560, 9728, 5)
+    x = synth.activations(1, 9728, 6)
+    w = pack_dev(f)
+    assert np.array_equal(run_gemv(f, x, w=w), run_gemv(f, x, w=w))
+
+
+def test_gemv_leaves_neighbouring_memory_alone():
+    f = synth.q4k_fields(37, 512, 8)
+    x = torch.from_numpy(synth.activations(2, 512, 9)).cuda()
+    w = pack_dev(f)
+    guard = torch.full((2 * 37 + 64,), 12345.0, device="cuda")
+    y = guard[32:32 + 2 * 37].view(2, 37)
+    q4k.q4k_gemv(w, 37, 512, x, y=y)
+    g = host(guard)
+    assert np.all(g[:32] == 12345.0) and np.all(g[32 + 74:] == 12345.0)
+
+
+# ------------------------------------------------------------------ GEMM
+def quantize_dev(x):
+    q, d8, s = q4k.q8_quantize(torch.from_numpy(x).cuda())
+    return q, d8, s
+
+
+@pytest.mark.parametrize("tokens,rows,cols", [
+    (1, 64, 256), (5, 70, 512), (64, 128, 2560), (130, 200, 768), (33, 9, 4096)])
+def test_gemm_parity_and_block_dots(tokens, rows, cols):
+    f = synth.q4k_fields(rows, cols, [tokens, rows, cols])
+    x = synth.activations(tokens, cols, [cols, tokens])
+    w = pack_dev(f)
+    q, d8, s = quantize_dev(x)
+    y = host(q4k.q4k_gemm(w, rows, cols, q, d8, s))
+    rq, rd, rs = O.quantize_q8_1(x)
+    y_ref, norm = O.mmq(f, rq, rd, rs)
+    assert_close(y, y_ref, norm, f"gemm {tokens}x{rows}x{cols}")
+    p = host(q4k.q4k_gemm_blockdots(w, rows, cols, q))
+    assert np.array_equal(p, O.block_dots(f["q"], rq))
+
+
+def test_gemm_block_dots_at_the_extremes():
+    # q = 15 against q8 = +-127 everywhere: the largest block dots there are
+    rows, cols, tokens = 16, 512, 8
+    f = synth.q4k_fields(rows, cols, 90)
+    f["q"][:] = 15
+    f["q"][::3, ::7] = 0
+    x = np.full((tokens, cols), 1.0, np.float32)
+    x[1::2] = -1.0
+    x[:, ::5] *= -1.0
+    w = pack_dev(f)
+    q, _, _ = quantize_dev(x)
+    p = host(q4k.q4k_gemm_blockdots(w, rows, cols, q))
+    assert np.array_equal(p, O.block_dots(f["q"], O.quantize_q8_1(x)[0]))
+    assert np.abs(p).max() == 15 * 127 * 32
+
+
+def test_gemm_prefill_512_sampled():
+    fields, xs = synth.prefill_4b_512()
+    rng = np.random.default_rng(123)
+    for name, inp in (("gate", "mlp_in"), ("down", "down_in")):
+        f, x = fields[name], xs[inp]
+        rows, cols = f["q"].shape
+        w = pack_dev(f)
+        q, d8, s = quantize_dev(x)
+        y = host(q4k.q4k_gemm(w, rows, cols, q, d8, s))
+        rq, rd, rs = O.quantize_q8_1(x)
+        sample = np.sort(rng.choice(rows, 256, replace=False))
+        y_ref, norm = O.mmq(slice_rows(f, sample), rq, rd, rs)
+        assert_close(y[:, sample], y_ref, norm, f"{name} rows sample")
+        toks = np.sort(rng.choice(512, 16, replace=False))
+        y_ref, norm = O.mmq(f, rq[toks], rd[toks], rs[toks])
+        assert_close(y[toks], y_ref, norm, f"{name} token sample")

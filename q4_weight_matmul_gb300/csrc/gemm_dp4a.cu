@@ -55,11 +55,13 @@ __global__ void __launch_bounds__(256) gemm_dp4a_kernel(
         val = reinterpret_cast<const uint4*>(q8 + (size_t)(tok0 + t) * cols + s * kQK)[v];
       *reinterpret_cast<uint4*>(s_q8 + t * kQ8Stride + 16 * v) = val;
     }
-    for (int i = tid; i < kTile * 8; i += 256) {
-      const int t = i >> 3, j = i & 7;
-      const bool ok = tok0 + t < tokens;
-      s_d8[t][j] = ok ? d8[(size_t)(tok0 + t) * (cols / kSub) + s * 8 + j] : 0.0f;
-      s_sum[t][j] = ok ? ssum[(size_t)(tok0 + t) * (cols / kSub) + s * 8 + j] : 0;
+    if (!p_out) {   // scales are not passed (null) when only block dots are wanted
+      for (int i = tid; i < kTile * 8; i += 256) {
+        const int t = i >> 3, j = i & 7;
+        const bool ok = tok0 + t < tokens;
+        s_d8[t][j] = ok ? d8[(size_t)(tok0 + t) * (cols / kSub) + s * 8 + j] : 0.0f;
+        s_sum[t][j] = ok ? ssum[(size_t)(tok0 + t) * (cols / kSub) + s * 8 + j] : 0;
+      }
     }
     __syncthreads();
     for (int i = tid; i < kTile * 8; i += 256) {

@@ -205,9 +205,16 @@ cudaError_t launch_b(const uint8_t* w, int rows, int nb, const float* x,
   cudaGetDevice(&dev);
   const DeviceInfo& info = device_info(dev);
   const size_t smem = smem_bytes(B, nb);
-  cudaError_t e = cudaFuncSetAttribute(gemv_block144_kernel<B>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  // raise the kernel's dynamic shared-memory limit once per device (it only grows)
+  static int s_limit[64];
+  int& limit = s_limit[dev & 63];
+  if ((int)smem > limit) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_block144_kernel<B>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         info.max_smem_optin);
+    if (e != cudaSuccess) return e;
+    limit = info.max_smem_optin;
+  }
   const int n_groups = (rows + 7) / 8;
   // split K across warps until every SM has a full CTA of work
   int ks = 1;

@@ -150,19 +150,20 @@ def test_gemm_parity_and_block_dots(tokens, rows, cols):
 
 
 def test_gemm_block_dots_at_the_extremes():
-    # q = 15 against q8 = +-127 everywhere: the largest block dots there are
+    # rows 0-7 hold q = 15 everywhere and tokens 0-3 are all +1 or all -1, so
+    # those block dots reach the extreme +-15*127*32; the rest are mixed.
     rows, cols, tokens = 16, 512, 8
     f = synth.q4k_fields(rows, cols, 90)
-    f["q"][:] = 15
-    f["q"][::3, ::7] = 0
+    f["q"][:8] = 15
+    f["q"][8:, ::7] = 0
     x = np.full((tokens, cols), 1.0, np.float32)
-    x[1::2] = -1.0
-    x[:, ::5] *= -1.0
+    x[1:4:2] = -1.0
+    x[4:, ::5] *= -1.0
     w = pack_dev(f)
     q, _, _ = quantize_dev(x)
     p = host(q4k.q4k_gemm_blockdots(w, rows, cols, q))
     assert np.array_equal(p, O.block_dots(f["q"], O.quantize_q8_1(x)[0]))
-    assert np.abs(p).max() == 15 * 127 * 32
+    assert p.max() == 15 * 127 * 32 and p.min() == -15 * 127 * 32
 
 
 def test_gemm_prefill_512_sampled():

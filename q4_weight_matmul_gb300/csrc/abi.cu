@@ -140,8 +140,16 @@ static int gemm_common(const void* w, int layout, int64_t rows, int64_t cols, co
   if (!aligned16(w) || !aligned16(q8) || (d8 && !aligned16(d8)) || (sum && !aligned16(sum)) ||
       (y && !aligned16(y)) || (p && !aligned16(p)))
     return Q4K_ERR_ALIGNMENT;
-  cudaError_t e = launch_gemm_dp4a(static_cast<const uint8_t*>(w), rows, cols, q8, d8, sum, tokens,
-                                   y, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (gemm_tc_supported(tokens)) {
+    int* err = device_error_word();
+    if (!err) return record_cuda(cudaGetLastError());
+    e = launch_gemm_block144(static_cast<const uint8_t*>(w), rows, cols, q8, d8, sum, tokens, y, p,
+                             err, static_cast<cudaStream_t>(stream));
+  } else {
+    e = launch_gemm_dp4a(static_cast<const uint8_t*>(w), rows, cols, q8, d8, sum, tokens, y, p,
+                         static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? Q4K_OK : record_cuda(e);
 }
 

@@ -2,38 +2,41 @@
 // BLOCK144 Q4_K weights (genie-ai-runtime §4, Path C: packed quants read as
 // whole words, dequantised in registers, residual folded in).
 //
-// Mapping.  One CTA of 1024 threads per SM (persistent).  A warp owns 8 rows;
-// lane (r, c) = (lane/4, lane%4) handles row r and the 64-weight chunk c of
-// every superblock it visits: its 32 quant bytes hold all of sub-block 2c
-// (low nibbles) and sub-block 2c+1 (high nibbles).  Warps split K when there
-// are too few rows to fill the machine (KS warps per 8-row group, summed in
-// shared memory in a fixed order, so results are bitwise deterministic).
+// Streaming.  One persistent CTA of 16 warps per SM.  Each warp owns a ring
+// of kRing shared-memory stages; one stage holds one superblock (144 bytes)
+// of each of the warp's 8 rows, fetched by eight cp.async.bulk copies that
+// complete on the stage's mbarrier.  The first copies are issued before the
+// activations are staged, so the weight stream starts at launch; afterwards a
+// stage is refilled as soon as the warp has consumed it.  Bytes in flight are
+// then set by the ring depth, not by registers.
 //
-// Dequantisation cost.  A nibble at bit position p (p <= 16) ORed into the
-// float 2^23 gives 2^23 + q*2^p exactly; subtracting 2^23 leaves q*2^p, and
-// the activation staged for that position is pre-multiplied by 2^-p, so the
-// product is exactly q*x before its usual fp32 rounding.  Eight nibbles of a
-// word need one shift, eight LOP3s, four packed fp32x2 adds and four packed
-// fp32x2 FMAs per token.  Each sub-block's partial sum is then scaled:
+// Mapping.  Lane (r, c) = (lane/4, lane%4) works on row r and the 64-weight
+// chunk c of each superblock: its 32 quant bytes hold all of sub-block 2c
+// (low nibbles) and all of sub-block 2c+1 (high nibbles).  When there are too
+// few 8-row groups to occupy every warp, ks warps split a group's superblocks
+// and their partial sums are added in shared memory in a fixed order, so the
+// result is bitwise deterministic.
+//
+// Dequantisation.  A nibble at bit position p (p <= 16) ORed into the float
+// 2^23 gives 2^23 + q*2^p exactly; subtracting 2^23 leaves q*2^p, and the
+// activation staged for that position is pre-multiplied by 2^-p, so the
+// product is exactly q*x before its fp32 rounding.  A word of eight nibbles
+// costs one shift, eight LOP3s, four fp32x2 adds and four fp32x2 FMAs per
+// token.  Each sub-block's partial dot is then scaled:
 //   acc += d*(sc_lo*S_lo + sc_hi*S_hi) - dmin*(m_lo*X_lo + m_hi*X_hi)
-// where X_j = sum of x over sub-block j (staged once per CTA).
+// with X_j the sum of x over sub-block j (staged once per CTA).
 #include "q4k_internal.h"
+#include "tc_ptx.cuh"
 
 #include <cuda_fp16.h>
 
 namespace q4k {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRegion = 68;   // floats per (token, superblock, chunk): 32 (lo,hi) pairs + pad
-
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
+constexpr int kRegion = 68;          // floats per (token, superblock, chunk): 32 (lo,hi) pairs + pad
+constexpr int kStageBytes = 8 * kBlockBytes;
 
 __device__ __forceinline__ float magic(uint32_t bits) { return __uint_as_float(0x4B000000u | bits); }
 
@@ -45,85 +48,139 @@ __device__ __forceinline__ int nib_shift(int l, int hi) {
   return (int)(((hi ? hi_tab : lo_tab) >> (8 * (l & 3))) & 0xFFu);
 }
 
+struct Layout {
+  int B, nb, ring;
+  size_t xs, xsum, red, stages, bars, total;
+};
+
+__host__ __device__ inline Layout layout(int B, int nb, int ring) {
+  Layout L;
+  L.B = B;
+  L.nb = nb;
+  L.ring = ring;
+  L.xs = 0;
+  L.xsum = L.xs + sizeof(float) * (size_t)B * nb * 4 * kRegion;
+  L.red = L.xsum + sizeof(float) * (size_t)B * nb * 8;
+  L.stages = (L.red + sizeof(float) * (size_t)kWarps * 8 * B + 127) & ~size_t(127);
+  L.bars = L.stages + (size_t)kWarps * ring * kStageBytes;
+  L.total = L.bars + sizeof(uint64_t) * kWarps * ring;
+  return L;
+}
+
 template <int B>
 __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
-    const uint4* __restrict__ w, int rows, int nb, int ks,
+    const uint8_t* __restrict__ w, int rows, int nb, int ks, int ring,
     const float* __restrict__ x, const float* __restrict__ residual,
-    float* __restrict__ y) {
-  extern __shared__ __align__(16) float smem[];
-  float* xs = smem;                                  // [B][nb][4][kRegion]
-  float* xsum = xs + (size_t)B * nb * 4 * kRegion;   // [B][nb*8]
-  float* red = xsum + (size_t)B * nb * 8;            // [kWarps][8][B]
+    float* __restrict__ y, int* __restrict__ err) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Layout L = layout(B, nb, ring);
+  float* xs = reinterpret_cast<float*>(smem + L.xs);
+  float* xsum = reinterpret_cast<float*>(smem + L.xsum);
+  float* red = reinterpret_cast<float*>(smem + L.red);
   const int cols = nb * kQK;
   const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int r8 = lane >> 2, c = lane & 3;
+  const int gpc = kWarps / ks;                       // 8-row groups per CTA pass
+  const int g = warp / ks, z = warp - g * ks;
+  const int n_groups = (rows + 7) >> 3;
+  const int stride = gridDim.x * gpc;
+  const int first = blockIdx.x * gpc;
+  const int n_pass = first < n_groups ? (n_groups - first + stride - 1) / stride : 0;
+  const int per_group = z < nb ? (nb - z + ks - 1) / ks : 0;   // superblocks of this warp per group
+  const int n_items = n_pass * per_group;
+  uint8_t* ring_base = smem + L.stages + (size_t)warp * ring * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars) + warp * ring;
+
+  if (lane == 0) {
+    for (int i = 0; i < ring; ++i) tc::mbar_init(&bars[i], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  // item j of this warp -> group and superblock
+  auto item_group = [&](int j) { return first + (j / per_group) * stride + g; };
+  auto item_sb = [&](int j) { return z + (j % per_group) * ks; };
+  auto issue = [&](int j) {
+    const int grp = item_group(j), sb = item_sb(j);
+    const int slot = j % ring;
+    int n_rows = 0;
+    if (grp < n_groups) n_rows = min(8, rows - grp * 8);
+    if (lane == 0) tc::mbar_arrive_expect_tx(&bars[slot], (uint32_t)(n_rows * kBlockBytes));
+    __syncwarp();
+    if (lane < n_rows) {
+      const size_t row = (size_t)grp * 8 + lane;
+      tc::bulk_g2s(ring_base + slot * kStageBytes + lane * kBlockBytes,
+                   w + (row * nb + sb) * kBlockBytes, kBlockBytes, &bars[slot]);
+    }
+  };
+
+  const int prime = n_items < ring ? n_items : ring;
+  for (int j = 0; j < prime; ++j) issue(j);
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // Stage the activations: pre-scaled by 2^-p and paired (lo, hi) per chunk.
   for (int i = tid; i < B * cols; i += kThreads) {
     const int b = i / cols, k = i - b * cols;
-    const int s = k >> 8, r = k & 255, c = r >> 6, t = r & 63;
+    const int s = k >> 8, r = k & 255, cc = r >> 6, t = r & 63;
     const int hi = t >> 5, l = t & 31;
     const float scale = __uint_as_float((uint32_t)(127 - nib_shift(l, hi)) << 23);
-    xs[(((size_t)b * nb + s) * 4 + c) * kRegion + 2 * l + hi] = x[(size_t)b * cols + k] * scale;
+    xs[(((size_t)b * nb + s) * 4 + cc) * kRegion + 2 * l + hi] = x[(size_t)b * cols + k] * scale;
   }
-  for (int i = tid; i < B * nb * 8; i += kThreads) {
-    const int b = i / (nb * 8), j = i - b * nb * 8;
-    const float* xp = x + (size_t)b * cols + 32 * j;
-    float acc = 0.0f;
-    for (int t = 0; t < 32; ++t) acc += xp[t];
-    xsum[i] = acc;
+  // Sums of x over each 32-wide sub-block (fixed order: 8 lanes x 4 values).
+  for (int i = warp; i < B * nb * 8 / 4; i += kWarps) {
+    const int base = 4 * i;            // four sub-blocks per warp pass, 8 lanes each
+    const int sbk = base + (lane >> 3);
+    const int b = sbk / (nb * 8), j = sbk - b * nb * 8;
+    const float4 v = *reinterpret_cast<const float4*>(x + (size_t)b * cols + 32 * j + 4 * (lane & 7));
+    float sum = (v.x + v.y) + (v.z + v.w);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    if ((lane & 7) == 0) xsum[sbk] = sum;
   }
   __syncthreads();
 
-  const int warp = tid >> 5, lane = tid & 31;
-  const int r8 = lane >> 2, c = lane & 3;
-  const int groups_per_cta = kWarps / ks;
-  const int g = warp / ks, z = warp - g * ks;
-  const int n_groups = (rows + 7) >> 3;
+  // lane-constant masks for the scale/min decode of sub-blocks 2c, 2c+1
   const int sh = (c & 1) * 16;
+  const uint32_t mA = c < 2 ? 0x3F3Fu : 0u, mB = c < 2 ? 0u : 0x0F0Fu, mC = c < 2 ? 0u : 0x3030u;
   const float2 kMagic2 = make_float2(-8388608.0f, -8388608.0f);
+  int zero = 0;
+  bool ok = true;
 
-  for (int base = blockIdx.x * groups_per_cta; base < n_groups; base += gridDim.x * groups_per_cta) {
-    const int grp = base + g;
+  int j = 0;
+  for (int pass = 0; pass < n_pass; ++pass) {
+    const int grp = first + pass * stride + g;
     const int row = grp * 8 + r8;
-    const bool valid = (grp < n_groups) && (row < rows);
-    const uint4* wrow = w + (size_t)(valid ? row : 0) * nb * 9;
+    const bool valid = grp < n_groups && row < rows;
     float acc[B];
 #pragma unroll
     for (int b = 0; b < B; ++b) acc[b] = 0.0f;
-
-    uint4 hd = make_uint4(0, 0, 0, 0), q0 = hd, q1 = hd;
-    if (valid && z < nb) {
-      hd = ld_stream(wrow + z * 9);
-      q0 = ld_stream(wrow + z * 9 + 1 + 2 * c);
-      q1 = ld_stream(wrow + z * 9 + 2 + 2 * c);
-    }
-    for (int s = z; s < nb; s += ks) {
-      uint4 hdn = make_uint4(0, 0, 0, 0), q0n = hdn, q1n = hdn;
-      if (valid && s + ks < nb) {
-        const uint4* p = wrow + (s + ks) * 9;
-        hdn = ld_stream(p);
-        q0n = ld_stream(p + 1 + 2 * c);
-        q1n = ld_stream(p + 2 + 2 * c);
+    for (int t = 0; t < per_group; ++t, ++j) {
+      const int slot = j % ring;
+      const int sb = item_sb(j);
+      if (ok && !tc::mbar_wait(&bars[slot], (uint32_t)((j / ring) & 1), &zero)) {
+        ok = false;
+        if (lane == 0) atomicOr(err, 2);
       }
-      // scales and mins of sub-blocks 2c (lo) and 2c+1 (hi)
+      const uint8_t* st = ring_base + slot * kStageBytes + r8 * kBlockBytes;
+      const uint4 hd = *reinterpret_cast<const uint4*>(st);
+      const uint4 q0 = *reinterpret_cast<const uint4*>(st + 16 + 32 * c);
+      const uint4 q1 = *reinterpret_cast<const uint4*>(st + 32 + 32 * c);
       const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
       const uint32_t a1 = hd.y >> sh, a2 = hd.z >> sh, a3 = hd.w >> sh;
-      uint32_t sc01, m01;
-      if (c < 2) {
-        sc01 = a1 & 0x3F3Fu;
-        m01 = a2 & 0x3F3Fu;
-      } else {
-        sc01 = (a3 & 0x0F0Fu) | ((a1 >> 2) & 0x3030u);
-        m01 = ((a3 >> 4) & 0x0F0Fu) | ((a2 >> 2) & 0x3030u);
-      }
+      const uint32_t sc01 = (a1 & mA) | (a3 & mB) | ((a1 >> 2) & mC);
+      const uint32_t m01 = (a2 & mA) | ((a3 >> 4) & mB) | ((a2 >> 2) & mC);
       const float sc_lo = (float)(sc01 & 0xFFu), sc_hi = (float)(sc01 >> 8);
       const float m_lo = (float)(m01 & 0xFFu), m_hi = (float)(m01 >> 8);
 
-      float2 part[B];
+      float2 pe[B], po[B];
 #pragma unroll
-      for (int b = 0; b < B; ++b) part[b] = make_float2(0.0f, 0.0f);
+      for (int b = 0; b < B; ++b) {
+        pe[b] = make_float2(0.0f, 0.0f);
+        po[b] = make_float2(0.0f, 0.0f);
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint4 qq = h ? q1 : q0;
@@ -138,26 +195,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
 #pragma unroll
           for (int b = 0; b < B; ++b) {
             const float4* xp = reinterpret_cast<const float4*>(
-                xs + (((size_t)b * nb + s) * 4 + c) * kRegion + 2 * (16 * h + 4 * k));
+                xs + (((size_t)b * nb + sb) * 4 + c) * kRegion + 2 * (16 * h + 4 * k));
             const float4 xa = xp[0], xb = xp[1];
-            part[b] = __ffma2_rn(f0, make_float2(xa.x, xa.y), part[b]);
-            part[b] = __ffma2_rn(f1, make_float2(xa.z, xa.w), part[b]);
-            part[b] = __ffma2_rn(f2, make_float2(xb.x, xb.y), part[b]);
-            part[b] = __ffma2_rn(f3, make_float2(xb.z, xb.w), part[b]);
+            pe[b] = __ffma2_rn(f0, make_float2(xa.x, xa.y), pe[b]);
+            po[b] = __ffma2_rn(f1, make_float2(xa.z, xa.w), po[b]);
+            pe[b] = __ffma2_rn(f2, make_float2(xb.x, xb.y), pe[b]);
+            po[b] = __ffma2_rn(f3, make_float2(xb.z, xb.w), po[b]);
           }
         }
       }
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        const float2 xsm = *reinterpret_cast<const float2*>(xsum + (size_t)b * nb * 8 + s * 8 + 2 * c);
-        const float scaled = fmaf(sc_hi, part[b].y, sc_lo * part[b].x);
+        const float2 part = __fadd2_rn(pe[b], po[b]);
+        const float2 xsm = *reinterpret_cast<const float2*>(xsum + (size_t)b * nb * 8 + sb * 8 + 2 * c);
+        const float scaled = fmaf(sc_hi, part.y, sc_lo * part.x);
         const float mins = fmaf(m_hi, xsm.y, m_lo * xsm.x);
         acc[b] = fmaf(dm.x, scaled, acc[b]);
         acc[b] = fmaf(-dm.y, mins, acc[b]);
       }
-      hd = hdn;
-      q0 = q0n;
-      q1 = q1n;
+      // every lane has used its words of this stage: hand it back to the copy engine
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (j + ring < n_items) issue(j + ring);
     }
 #pragma unroll
     for (int b = 0; b < B; ++b) {
@@ -165,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
       acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 2);
     }
     if (ks == 1) {
-      if (valid && c == 0) {
+      if (valid && c == 0 && ok) {
 #pragma unroll
         for (int b = 0; b < B; ++b) {
           float v = acc[b];
@@ -179,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
         for (int b = 0; b < B; ++b) red[(warp * 8 + r8) * B + b] = acc[b];
       }
       __syncthreads();
-      if (z == 0 && c == 0 && valid) {
+      if (z == 0 && c == 0 && valid && ok) {
 #pragma unroll
         for (int b = 0; b < B; ++b) {
           float v = 0.0f;
@@ -194,8 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-size_t smem_bytes(int batch, int nb) {
-  return sizeof(float) * ((size_t)batch * nb * (4 * kRegion + 8) + (size_t)kWarps * 8 * batch);
+int pick_ring(int batch, int nb, int smem_optin) {
+  for (int ring = 4; ring >= 2; --ring)
+    if (layout(batch, nb, ring).total <= (size_t)smem_optin) return ring;
+  return 0;
 }
 
 template <int B>
@@ -204,26 +265,29 @@ cudaError_t launch_b(const uint8_t* w, int rows, int nb, const float* x,
   int dev = 0;
   cudaGetDevice(&dev);
   const DeviceInfo& info = device_info(dev);
-  const size_t smem = smem_bytes(B, nb);
-  // raise the kernel's dynamic shared-memory limit once per device (it only grows)
+  const int ring = pick_ring(B, nb, info.max_smem_optin);
+  if (ring == 0) return cudaErrorNotSupported;
+  const size_t smem = layout(B, nb, ring).total;
+  // raise the kernel's dynamic shared-memory limit once per device
   static int s_limit[64];
   int& limit = s_limit[dev & 63];
-  if ((int)smem > limit) {
+  if (limit < info.max_smem_optin) {
     cudaError_t e = cudaFuncSetAttribute(gemv_block144_kernel<B>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          info.max_smem_optin);
     if (e != cudaSuccess) return e;
     limit = info.max_smem_optin;
   }
+  int* err = device_error_word();
+  if (!err) return cudaErrorInvalidValue;
   const int n_groups = (rows + 7) / 8;
   // split K across warps until every SM has a full CTA of work
   int ks = 1;
-  while (ks < 8 && ks * 2 <= nb && (int64_t)n_groups * ks < (int64_t)info.sm_count * kWarps) ks *= 2;
-  const int groups_per_cta = kWarps / ks;
-  int grid = (n_groups + groups_per_cta - 1) / groups_per_cta;
+  while (ks < kWarps && ks * 2 <= nb && (int64_t)n_groups * ks < (int64_t)info.sm_count * kWarps) ks *= 2;
+  const int gpc = kWarps / ks;
+  int grid = (n_groups + gpc - 1) / gpc;
   if (grid > info.sm_count) grid = info.sm_count;
-  gemv_block144_kernel<B><<<grid, kThreads, smem, s>>>(
-      reinterpret_cast<const uint4*>(w), rows, nb, ks, x, residual, y);
+  gemv_block144_kernel<B><<<grid, kThreads, smem, s>>>(w, rows, nb, ks, ring, x, residual, y, err);
   return cudaGetLastError();
 }
 
@@ -233,7 +297,7 @@ bool gemv_supported(int64_t cols, int batch) {
   if (batch < 1 || batch > 8) return false;
   int dev = 0;
   cudaGetDevice(&dev);
-  return smem_bytes(batch, (int)(cols / kQK)) <= (size_t)device_info(dev).max_smem_optin;
+  return pick_ring(batch, (int)(cols / kQK), device_info(dev).max_smem_optin) != 0;
 }
 
 cudaError_t launch_gemv_block144(const uint8_t* w, int64_t rows, int64_t cols,

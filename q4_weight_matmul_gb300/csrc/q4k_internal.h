@@ -47,8 +47,10 @@ cudaError_t launch_gemm_dp4a(const uint8_t* w, int64_t rows, int64_t cols,
                              const int32_t* sum, int64_t tokens, float* y,
                              int32_t* p_out, cudaStream_t s);
 
-// Prefill MMQ GEMM.  When `p_out` is non-null the kernel stores the raw
-// per-block integer dots there instead of y (test export).
+// Tensor-core prefill MMQ GEMM (tcgen05).  When `p_out` is non-null the
+// kernel stores the raw per-block integer dots there instead of y (test
+// export); `err` is the device error word a timed-out wait sets.
+bool gemm_tc_supported(int64_t tokens);
 cudaError_t launch_gemm_block144(const uint8_t* w, int64_t rows, int64_t cols,
                                  const int8_t* q8, const float* d8,
                                  const int32_t* sum, int64_t tokens, float* y,

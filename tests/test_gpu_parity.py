@@ -134,8 +134,10 @@ def quantize_dev(x):
     return q, d8, s
 
 
+# token counts below 16 run the dp4a kernel, the rest the tensor-core kernel
 @pytest.mark.parametrize("tokens,rows,cols", [
-    (1, 64, 256), (5, 70, 512), (64, 128, 2560), (130, 200, 768), (33, 9, 4096)])
+    (1, 64, 256), (5, 70, 512), (15, 33, 768), (16, 128, 256), (40, 64, 256), (64, 128, 2560),
+    (130, 200, 768), (33, 9, 4096), (200, 300, 1280), (129, 257, 512)])
 def test_gemm_parity_and_block_dots(tokens, rows, cols):
     f = synth.q4k_fields(rows, cols, [tokens, rows, cols])
     x = synth.activations(tokens, cols, [cols, tokens])

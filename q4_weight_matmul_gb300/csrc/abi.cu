@@ -3,7 +3,9 @@
 // here allocates device memory; the only device state the library owns is a
 // per-device error word that kernels with bounded waits set when they give up.
 #include "q4k_internal.h"
+#include "tmap.h"
 
+#include <cudaTypedefs.h>
 #include <q4k.h>
 
 #include <cstdio>
@@ -70,6 +72,31 @@ int* device_error_word() {
     g_error_ptr[dev] = static_cast<int*>(p);
   }
   return g_error_ptr[dev];
+}
+
+bool encode_tmap_u8_3d(CUtensorMap* map, const void* base, const uint64_t dims[3],
+                       const uint64_t strides[2], const uint32_t box[3]) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const cuuint64_t gdim[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t gstride[2] = {strides[0], strides[1]};
+  const cuuint32_t bdim[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gdim, gstride,
+                      bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 }  // namespace q4k

@@ -2,34 +2,39 @@
 // BLOCK144 Q4_K weights (genie-ai-runtime §4, Path C: packed quants read as
 // whole words, dequantised in registers, residual folded in).
 //
-// Streaming.  One persistent CTA per SM: a producer warp and 16 consumer
-// warps.  The matrix is cut into tiles of `tr` rows; a tile streams through a
-// ring of shared-memory stages, each stage one TMA box of tr rows x S
-// superblocks (tr * S = 128, 18 KB), fetched by a single 3-D tensor copy with
-// out-of-range rows and superblocks zero-filled.  The producer starts the
-// stream at launch, before the activations are staged, and keeps every free
-// stage filled; bytes in flight are set by the ring, not by registers.
+// Work split.  Rows are cut into blocks of RB rows (RB = 32, 16 or 8, the
+// largest that still gives every SM a block); one CTA per SM owns a run of
+// row blocks and all their superblocks.  A unit of work is one row block x
+// one superblock; the 16 consumer warps of a CTA take units round-robin, so
+// every warp streams several superblocks and K is split across warps.  Each
+// unit leaves one partial sum per row in shared memory; at the end the CTA
+// adds a row's partials in superblock order (bitwise deterministic).
 //
-// Mapping.  Consumer warp (g, z) owns 8-row group g of the tile and superblock
-// z of each stage; lane (r, c) = (lane/4, lane%4) works on row r and the
-// 64-weight chunk c of that superblock (its 32 quant bytes hold all of
-// sub-block 2c in low nibbles and 2c+1 in high nibbles).  The S partial sums of
-// a group are added in shared memory in a fixed order, so results are
-// bitwise deterministic.
+// Streaming.  A producer warp fetches the CTA's weights with 3-D tensor
+// copies: one copy per stage of RB rows x (128/RB) superblocks (18 KB, out of
+// range rows and superblocks zero-filled) into a ring of stages.  It starts
+// at launch, before the activations are staged, so bytes in flight are set by
+// the ring, not by registers.
+//
+// Lanes.  32/RB lanes share a row: with RB = 32 a lane owns a row's whole
+// superblock (256 weights), with RB = 16 half of it, with RB = 8 one 64-weight
+// chunk.  A chunk's 32 quant bytes hold sub-block 2c in low nibbles and 2c+1
+// in high nibbles, so scale/min decoding is paid once per 64-256 weights.
 //
 // Dequantisation.  A nibble at bit position p (p <= 16) ORed into the float
 // 2^23 gives 2^23 + q*2^p exactly; subtracting 2^23 leaves q*2^p, and the
 // activation staged for that position is pre-multiplied by 2^-p, so the
 // product is exactly q*x before its fp32 rounding.  A word of eight nibbles
-// costs one shift, eight LOP3s, four fp32x2 adds and four fp32x2 FMAs per
-// token.  Each sub-block's partial dot is then scaled:
-//   acc += d*(sc_lo*S_lo + sc_hi*S_hi) - dmin*(m_lo*X_lo + m_hi*X_hi)
-// with X_j the sum of x over sub-block j (staged once per CTA).
+// costs one shift, eight LOP3s, four fp32x2 adds and four fp32x2 FMAs (per
+// token), written in PTX so that the pairs are formed in place.  Per
+// sub-block j:  acc += d*sc_j*P_j - dmin*m_j*X_j  with X_j = sum of x over j.
 #include "q4k_internal.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
 
 #include <cuda_fp16.h>
+
+#include <cstdint>
 
 namespace q4k {
 namespace {
@@ -38,10 +43,9 @@ constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;     // + one producer warp
 constexpr int kRegion = 68;                   // floats per (token, superblock, chunk): 32 (lo,hi) pairs + pad
-constexpr int kStageSuper = 128;              // superblock-rows per stage (tr * S)
+constexpr int kStageSuper = 128;              // superblock-rows per stage (RB * SB)
 constexpr int kStageBytes = kStageSuper * kBlockBytes;
-
-__device__ __forceinline__ float magic(uint32_t bits) { return __uint_as_float(0x4B000000u | bits); }
+constexpr int kMaxRing = 8;
 
 // Power-of-two pre-scale exponent of weight l (0..31) of the low (hi = 0) or
 // high (hi = 1) half of a chunk; matches the nibble positions used below.
@@ -55,32 +59,81 @@ __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
 }
 
+// Eight nibbles of v -> four exact (q_lo*2^p, q_hi*2^p) fp32 pairs.
+__device__ __forceinline__ void conv_word(uint32_t v, uint64_t& f0, uint64_t& f1, uint64_t& f2,
+                                          uint64_t& f3) {
+  asm("{\n\t.reg .b32 a0,a1,a2,a3,a4,a5,a6,a7,v12;\n\t"
+      "shr.b32 v12, %4, 12;\n\t"
+      "lop3.b32 a0, %4, 0xF, 0x4B000000, 0xEA;\n\t"
+      "lop3.b32 a1, %4, 0xF0, 0x4B000000, 0xEA;\n\t"
+      "lop3.b32 a2, %4, 0xF00, 0x4B000000, 0xEA;\n\t"
+      "lop3.b32 a3, %4, 0xF000, 0x4B000000, 0xEA;\n\t"
+      "lop3.b32 a4, %4, 0xF0000, 0x4B000000, 0xEA;\n\t"
+      "lop3.b32 a5, v12, 0xF00, 0x4B000000, 0xEA;\n\t"
+      "lop3.b32 a6, v12, 0xF000, 0x4B000000, 0xEA;\n\t"
+      "lop3.b32 a7, v12, 0xF0000, 0x4B000000, 0xEA;\n\t"
+      "mov.b64 %0, {a0, a1};\n\tmov.b64 %1, {a2, a3};\n\tmov.b64 %2, {a4, a5};\n\tmov.b64 %3, {a6, a7};\n\t"
+      "add.rn.f32x2 %0, %0, %5;\n\tadd.rn.f32x2 %1, %1, %5;\n\t"
+      "add.rn.f32x2 %2, %2, %5;\n\tadd.rn.f32x2 %3, %3, %5;\n\t}"
+      : "=l"(f0), "=l"(f1), "=l"(f2), "=l"(f3)
+      : "r"(v), "l"(0xCB000000CB000000ull));
+}
+
+// pe += f0*x(0,1) + f2*x(4,5); po += f1*x(2,3) + f3*x(6,7)
+__device__ __forceinline__ void fma_word(uint64_t f0, uint64_t f1, uint64_t f2, uint64_t f3,
+                                         const uint4& xa, const uint4& xc, uint64_t& pe, uint64_t& po) {
+  asm("{\n\t.reg .b64 x0,x1,x2,x3;\n\t"
+      "mov.b64 x0, {%6, %7};\n\tmov.b64 x1, {%8, %9};\n\t"
+      "mov.b64 x2, {%10, %11};\n\tmov.b64 x3, {%12, %13};\n\t"
+      "fma.rn.f32x2 %0, %2, x0, %0;\n\tfma.rn.f32x2 %1, %3, x1, %1;\n\t"
+      "fma.rn.f32x2 %0, %4, x2, %0;\n\tfma.rn.f32x2 %1, %5, x3, %1;\n\t}"
+      : "+l"(pe), "+l"(po)
+      : "l"(f0), "l"(f1), "l"(f2), "l"(f3), "r"(xa.x), "r"(xa.y), "r"(xa.z), "r"(xa.w), "r"(xc.x),
+        "r"(xc.y), "r"(xc.z), "r"(xc.w));
+}
+
+__device__ __forceinline__ float2 u64_as_f2(uint64_t v) {
+  return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
+}
+
+// byte i of w as a float (exact)
+__device__ __forceinline__ float byte_f(uint32_t w, int i) { return (float)((w >> (8 * i)) & 0xFFu); }
+
 struct Layout {
-  size_t xs, xsum, red, stages, bars, total;
+  size_t xs, xsum, part, stages, bars, total;
 };
 
-__host__ __device__ inline Layout layout(int B, int nb, int ring) {
+__host__ __device__ inline Layout layout(int B, int nb, int ring, int part_floats) {
   Layout L;
   L.xs = 0;
   L.xsum = L.xs + sizeof(float) * (size_t)B * nb * 4 * kRegion;
-  L.red = L.xsum + sizeof(float) * (size_t)B * nb * 8;
-  L.stages = (L.red + sizeof(float) * (size_t)kConsumerWarps * 8 * B + 1023) & ~size_t(1023);
+  L.part = L.xsum + sizeof(float) * (size_t)B * nb * 8;
+  L.stages = (L.part + sizeof(float) * (size_t)part_floats + 1023) & ~size_t(1023);
   L.bars = L.stages + (size_t)ring * kStageBytes;
   L.total = L.bars + sizeof(uint64_t) * 2 * ring + 1024;   // + slack to align the base
   return L;
 }
 
-template <int B>
+// LPR: lanes per row (1, 2 or 4); RB = 32 / LPR rows per block.
+template <int B, int LPR>
 __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
-    const __grid_constant__ CUtensorMap tmap, int rows, int nb, int tr, int ring, int rows_inner,
+    const __grid_constant__ CUtensorMap tmap, int rows, int nb, int rb_per_cta, int ring,
     const float* __restrict__ x, const float* __restrict__ residual,
     float* __restrict__ y, int* __restrict__ err) {
+  constexpr int RB = 32 / LPR;              // rows per block
+  constexpr int SB = kStageSuper / RB;      // superblocks per stage
+  constexpr int CPL = 4 / LPR;              // 64-weight chunks per lane
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Layout L = layout(B, nb, ring);
+  const int n_rb = (rows + RB - 1) / RB;
+  const int rb0 = blockIdx.x * rb_per_cta;
+  const int my_rb = max(0, min(rb_per_cta, n_rb - rb0));
+  const int n_sj = (nb + SB - 1) / SB;      // stages per row block
+  const int n_stages = my_rb * n_sj;
+  const Layout L = layout(B, nb, ring, B * rb_per_cta * nb * RB);
   float* xs = reinterpret_cast<float*>(smem + L.xs);
   float* xsum = reinterpret_cast<float*>(smem + L.xsum);
-  float* red = reinterpret_cast<float*>(smem + L.red);
+  float* part = reinterpret_cast<float*>(smem + L.part);      // [B][rb][nb][RB]
   uint8_t* stages = smem + L.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ring;
@@ -88,14 +141,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
   const int cols = nb * kQK;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int S = kStageSuper / tr;                    // superblocks per stage
-  const int n_tiles = (rows + tr - 1) / tr;
-  const int n_st = (nb + S - 1) / S;                 // stages per tile
 
   if (tid == 0) {
     for (int i = 0; i < ring; ++i) {
       tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], kConsumerWarps);
+      tc::mbar_init(&empty[i], SB);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -105,23 +155,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap) : "memory");
-      int slot = 0;
+      int slot = 0, rb = 0, sj = 0;
       uint32_t phase = 0;
-      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        for (int st = 0; st < n_st; ++st) {
-          if (!tc::mbar_wait_sleep(&empty[slot], phase ^ 1)) {
-            atomicOr(err, 2);
-            return;
-          }
-          tc::mbar_arrive_expect_tx(&full[slot], kStageBytes);
-          if (rows_inner)
-            tc::tma_load_3d(stages + (size_t)slot * kStageBytes, &tmap, 0, tile * tr, st * S, &full[slot]);
-          else
-            tc::tma_load_3d(stages + (size_t)slot * kStageBytes, &tmap, 0, st * S, tile * tr, &full[slot]);
-          if (++slot == ring) {
-            slot = 0;
-            phase ^= 1;
-          }
+      for (int j = 0; j < n_stages; ++j) {
+        if (!tc::mbar_wait_sleep(&empty[slot], phase ^ 1)) {
+          atomicOr(err, 2);
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&full[slot], kStageBytes);
+        tc::tma_load_3d(stages + (size_t)slot * kStageBytes, &tmap, 0, (rb0 + rb) * RB, sj * SB, &full[slot]);
+        if (++sj == n_sj) {
+          sj = 0;
+          ++rb;
+        }
+        if (++slot == ring) {
+          slot = 0;
+          phase ^= 1;
         }
       }
     }
@@ -130,7 +179,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
 
   // -------------------------------------------------------------- consumers
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // Stage the activations: pre-scaled by 2^-p and paired (lo, hi) per chunk.
   for (int i = tid; i < B * cols; i += kConsumers) {
     const int b = i / cols, k = i - b * cols;
     const int s = k >> 8, r = k & 255, cc = r >> 6, t = r & 63;
@@ -138,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
     const float scale = __uint_as_float((uint32_t)(127 - nib_shift(l, hi)) << 23);
     xs[(((size_t)b * nb + s) * 4 + cc) * kRegion + 2 * l + hi] = x[(size_t)b * cols + k] * scale;
   }
-  // Sums of x over each 32-wide sub-block (fixed order: 8 lanes x 4 values).
   for (int i = warp; i < B * nb * 2; i += kConsumerWarps) {
     const int sbk = 4 * i + (lane >> 3);
     const int b = sbk / (nb * 8), j = sbk - b * nb * 8;
@@ -151,136 +198,158 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
   }
   named_sync_consumers();
 
-  const int g = warp / S, z = warp - g * S;
-  const int r8 = lane >> 2, c = lane & 3;
-  const int sh = (c & 1) * 16;
-  const uint32_t mA = c < 2 ? 0x3F3Fu : 0u, mB = c < 2 ? 0u : 0x0F0Fu, mC = c < 2 ? 0u : 0x3030u;
-  const float2 kMagic2 = make_float2(-8388608.0f, -8388608.0f);
-  // this lane's 144-byte superblock inside a stage laid out [S][tr][144]
-  // (rows inner) or [tr][S][144]
-  const size_t lane_off = rows_inner ? ((size_t)z * tr + g * 8 + r8) * kBlockBytes
-                                     : ((size_t)(g * 8 + r8) * S + z) * kBlockBytes;
+  const int r_in = lane / LPR;              // row inside the block
+  const int lq = lane % LPR;                // this lane's share of the superblock
+  const int c0 = lq * CPL;                  // first chunk of the lane
   bool ok = true;
-  int slot = 0;
-  uint32_t phase = 0;
-
-  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-    const int row = tile * tr + g * 8 + r8;
+  // units u = warp, warp + 16, ...: stage j = u / SB, superblock slot z = u % SB
+  const int n_units = n_stages * SB;
+  for (int u = warp; u < n_units; u += kConsumerWarps) {
+    const int j = u / SB, z = u - j * SB;
+    const int slot = j % ring;
+    const uint32_t phase = (uint32_t)((j / ring) & 1);
+    const int rbl = j / n_sj, sj = j - rbl * n_sj;
+    const int sb = sj * SB + z;
+    if (ok && !tc::mbar_wait_sleep(&full[slot], phase)) {
+      ok = false;
+      if (lane == 0) atomicOr(err, 2);
+    }
     float acc[B];
 #pragma unroll
     for (int b = 0; b < B; ++b) acc[b] = 0.0f;
-    for (int st = 0; st < n_st; ++st) {
-      const int sb = st * S + z;
-      if (ok && !tc::mbar_wait_sleep(&full[slot], phase)) {
-        ok = false;
-        if (lane == 0) atomicOr(err, 2);
-      }
-      if (sb < nb) {
-        const uint8_t* p = stages + (size_t)slot * kStageBytes + lane_off;
-        const uint4 hd = *reinterpret_cast<const uint4*>(p);
+    if (sb < nb) {
+      // stage laid out [SB][RB][144] (rows inner)
+      const uint8_t* p = stages + (size_t)slot * kStageBytes + ((size_t)z * RB + r_in) * kBlockBytes;
+      const uint4 hd = *reinterpret_cast<const uint4*>(p);
+      const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
+      // scales (sc) and mins (m) of sub-blocks 0..3 and 4..7, one byte each
+      const uint32_t sc03 = hd.y & 0x3F3F3F3Fu, m03 = hd.z & 0x3F3F3F3Fu;
+      const uint32_t sc47 = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+      const uint32_t m47 = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+      float scaled[B], mins[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) scaled[b] = mins[b] = 0.0f;
+#pragma unroll
+      for (int cc = 0; cc < CPL; ++cc) {
+        const int c = c0 + cc;
         const uint4 q0 = *reinterpret_cast<const uint4*>(p + 16 + 32 * c);
         const uint4 q1 = *reinterpret_cast<const uint4*>(p + 32 + 32 * c);
-        const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
-        const uint32_t a1 = hd.y >> sh, a2 = hd.z >> sh, a3 = hd.w >> sh;
-        const uint32_t sc01 = (a1 & mA) | (a3 & mB) | ((a1 >> 2) & mC);
-        const uint32_t m01 = (a2 & mA) | ((a3 >> 4) & mB) | ((a2 >> 2) & mC);
-        const float sc_lo = (float)(sc01 & 0xFFu), sc_hi = (float)(sc01 >> 8);
-        const float m_lo = (float)(m01 & 0xFFu), m_hi = (float)(m01 >> 8);
-
-        float2 pe[B], po[B];
+        uint64_t pe[B], po[B];
 #pragma unroll
-        for (int b = 0; b < B; ++b) {
-          pe[b] = make_float2(0.0f, 0.0f);
-          po[b] = make_float2(0.0f, 0.0f);
-        }
-        const float* xb0 = xs + ((size_t)sb * 4 + c) * kRegion;
+        for (int b = 0; b < B; ++b) pe[b] = po[b] = 0ull;
+        const float* xc0 = xs + ((size_t)sb * 4 + c) * kRegion;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint4 qq = h ? q1 : q0;
           const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t v = words[k], v12 = v >> 12;
-            const float2 f0 = __fadd2_rn(make_float2(magic(v & 0xFu), magic(v & 0xF0u)), kMagic2);
-            const float2 f1 = __fadd2_rn(make_float2(magic(v & 0xF00u), magic(v & 0xF000u)), kMagic2);
-            const float2 f2 = __fadd2_rn(make_float2(magic(v & 0xF0000u), magic(v12 & 0xF00u)), kMagic2);
-            const float2 f3 = __fadd2_rn(make_float2(magic(v12 & 0xF000u), magic(v12 & 0xF0000u)), kMagic2);
+            uint64_t f0, f1, f2, f3;
+            conv_word(words[k], f0, f1, f2, f3);
 #pragma unroll
             for (int b = 0; b < B; ++b) {
-              const float4* xp = reinterpret_cast<const float4*>(
-                  xb0 + (size_t)b * nb * 4 * kRegion + 2 * (16 * h + 4 * k));
-              const float4 xa = xp[0], xc = xp[1];
-              pe[b] = __ffma2_rn(f0, make_float2(xa.x, xa.y), pe[b]);
-              po[b] = __ffma2_rn(f1, make_float2(xa.z, xa.w), po[b]);
-              pe[b] = __ffma2_rn(f2, make_float2(xc.x, xc.y), pe[b]);
-              po[b] = __ffma2_rn(f3, make_float2(xc.z, xc.w), po[b]);
+              const uint4* xp = reinterpret_cast<const uint4*>(xc0 + (size_t)b * nb * 4 * kRegion + 2 * (16 * h + 4 * k));
+              fma_word(f0, f1, f2, f3, xp[0], xp[1], pe[b], po[b]);
             }
           }
         }
+        // sub-blocks 2c (low nibbles) and 2c+1 (high nibbles)
+        const uint32_t scw = c < 2 ? sc03 : sc47, mw = c < 2 ? m03 : m47;
+        const int bi = 2 * (c & 1);
+        const float sc_lo = byte_f(scw, bi), sc_hi = byte_f(scw, bi + 1);
+        const float m_lo = byte_f(mw, bi), m_hi = byte_f(mw, bi + 1);
 #pragma unroll
         for (int b = 0; b < B; ++b) {
-          const float2 part = __fadd2_rn(pe[b], po[b]);
+          const float2 a = u64_as_f2(pe[b]), o = u64_as_f2(po[b]);
           const float2 xsm = *reinterpret_cast<const float2*>(xsum + (size_t)b * nb * 8 + sb * 8 + 2 * c);
-          const float scaled = fmaf(sc_hi, part.y, sc_lo * part.x);
-          const float mins = fmaf(m_hi, xsm.y, m_lo * xsm.x);
-          acc[b] = fmaf(dm.x, scaled, acc[b]);
-          acc[b] = fmaf(-dm.y, mins, acc[b]);
+          scaled[b] = fmaf(sc_hi, a.y + o.y, fmaf(sc_lo, a.x + o.x, scaled[b]));
+          mins[b] = fmaf(m_hi, xsm.y, fmaf(m_lo, xsm.x, mins[b]));
         }
       }
-      // release the stage once every lane of the warp has read it
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&empty[slot]);
-      if (++slot == ring) {
-        slot = 0;
-        phase ^= 1;
-      }
+#pragma unroll
+      for (int b = 0; b < B; ++b) acc[b] = fmaf(dm.x, scaled[b], -dm.y * mins[b]);
     }
+    // release the stage once every lane of the warp has read it
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&empty[slot]);
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-      acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 1);
-      acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 2);
+      if (LPR >= 2) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 1);
+      if (LPR >= 4) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 2);
     }
-    const bool valid = row < rows && ok;
-    if (S == 1) {
-      if (valid && c == 0) {
+    if (lq == 0 && sb < nb) {
 #pragma unroll
-        for (int b = 0; b < B; ++b) {
-          float v = acc[b];
-          if (residual) v += residual[(size_t)b * rows + row];
-          y[(size_t)b * rows + row] = v;
-        }
-      }
-    } else {
-      if (c == 0) {
-#pragma unroll
-        for (int b = 0; b < B; ++b) red[(warp * 8 + r8) * B + b] = acc[b];
-      }
-      named_sync_consumers();
-      if (z == 0 && c == 0 && valid) {
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-          float v = 0.0f;
-          for (int zz = 0; zz < S; ++zz) v += red[((warp + zz) * 8 + r8) * B + b];
-          if (residual) v += residual[(size_t)b * rows + row];
-          y[(size_t)b * rows + row] = v;
-        }
-      }
-      named_sync_consumers();
+      for (int b = 0; b < B; ++b) part[(((size_t)b * rb_per_cta + rbl) * nb + sb) * RB + r_in] = acc[b];
+    }
+  }
+  named_sync_consumers();
+  // y = sum of a row's partials in superblock order (+ residual)
+  for (int i = tid; i < B * my_rb * RB; i += kConsumers) {
+    const int b = i / (my_rb * RB), rem = i - b * my_rb * RB;
+    const int rbl = rem / RB, r = rem - rbl * RB;
+    const int row = (rb0 + rbl) * RB + r;
+    if (row < rows && ok) {
+      const float* pp = part + (((size_t)b * rb_per_cta + rbl) * nb) * RB + r;
+      float v = 0.0f;
+      for (int s = 0; s < nb; ++s) v += pp[(size_t)s * RB];
+      if (residual) v += residual[(size_t)b * rows + row];
+      y[(size_t)b * rows + row] = v;
     }
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-int pick_ring(int batch, int nb, int smem_optin) {
-  for (int ring = 4; ring >= 2; --ring)
-    if (layout(batch, nb, ring).total <= (size_t)smem_optin) return ring;
-  return 0;
+struct Plan {
+  int lpr, rb_per_cta, grid, ring;
+  size_t smem;
+};
+
+Plan make_plan(int B, int64_t rows, int nb, const DeviceInfo& info) {
+  Plan p{};
+  // rows per block: the one whose busiest SM holds the fewest rows (ties go to
+  // the taller block, which decodes scales less often)
+  p.lpr = 4;
+  int64_t best = INT64_MAX;
+  for (int lpr = 1; lpr <= 4; lpr *= 2) {
+    const int64_t rb = 32 / lpr, n_rb = (rows + rb - 1) / rb;
+    const int64_t per = (n_rb + info.sm_count - 1) / info.sm_count;
+    if (per * rb < best) {
+      best = per * rb;
+      p.lpr = lpr;
+    }
+  }
+  const int RB = 32 / p.lpr;
+  const int n_rb = (int)((rows + RB - 1) / RB);
+  p.rb_per_cta = (n_rb + info.sm_count - 1) / info.sm_count;
+  p.grid = (n_rb + p.rb_per_cta - 1) / p.rb_per_cta;
+  p.ring = 0;
+  for (int ring = kMaxRing; ring >= 2; --ring) {
+    const size_t total = layout(B, nb, ring, B * p.rb_per_cta * nb * RB).total;
+    if (total <= (size_t)info.max_smem_optin) {
+      p.ring = ring;
+      p.smem = total;
+      break;
+    }
+  }
+  return p;
 }
 
-int pick_tile_rows(int64_t rows, int sm_count) {
-  for (int tr = kStageSuper; tr > 8; tr >>= 1)
-    if ((rows + tr - 1) / tr >= sm_count) return tr;
-  return 8;
+template <int B, int LPR>
+cudaError_t launch_bl(const CUtensorMap& map, int rows, int nb, const Plan& p, const float* x,
+                      const float* residual, float* y, int* err, int dev, const DeviceInfo& info,
+                      cudaStream_t s) {
+  static int s_limit[64];
+  int& limit = s_limit[dev & 63];
+  if (limit < info.max_smem_optin) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_block144_kernel<B, LPR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         info.max_smem_optin);
+    if (e != cudaSuccess) return e;
+    limit = info.max_smem_optin;
+  }
+  gemv_block144_kernel<B, LPR><<<p.grid, kThreads, p.smem, s>>>(map, rows, nb, p.rb_per_cta, p.ring, x,
+                                                                residual, y, err);
+  return cudaGetLastError();
 }
 
 template <int B>
@@ -289,44 +358,22 @@ cudaError_t launch_b(const uint8_t* w, int rows, int nb, const float* x,
   int dev = 0;
   cudaGetDevice(&dev);
   const DeviceInfo& info = device_info(dev);
-  const int ring = pick_ring(B, nb, info.max_smem_optin);
-  if (ring == 0) return cudaErrorNotSupported;
-  const size_t smem = layout(B, nb, ring).total;
-  static int s_limit[64];
-  int& limit = s_limit[dev & 63];
-  if (limit < info.max_smem_optin) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_block144_kernel<B>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         info.max_smem_optin);
-    if (e != cudaSuccess) return e;
-    limit = info.max_smem_optin;
-  }
+  const Plan p = make_plan(B, rows, nb, info);
+  if (p.ring == 0) return cudaErrorNotSupported;
   int* err = device_error_word();
   if (!err) return cudaErrorInvalidValue;
-  const int tr = pick_tile_rows(rows, info.sm_count);
-  const int S = kStageSuper / tr;
-  // Preferred box order: bytes, rows, superblocks (rows inner: conflict-free
-  // shared-memory reads); fall back to the memory order if the driver
-  // rejects the non-monotonic strides.
+  const int RB = 32 / p.lpr, SB = kStageSuper / RB;
+  // box: bytes of a superblock x RB rows x SB superblocks, rows inner in shared memory
   CUtensorMap map;
-  int rows_inner = 1;
-  {
-    const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)rows, (uint64_t)nb};
-    const uint64_t strides[2] = {(uint64_t)nb * kBlockBytes, (uint64_t)kBlockBytes};
-    const uint32_t box[3] = {(uint32_t)kBlockBytes, (uint32_t)tr, (uint32_t)S};
-    if (!encode_tmap_u8_3d(&map, w, dims, strides, box)) {
-      rows_inner = 0;
-      const uint64_t dims2[3] = {(uint64_t)kBlockBytes, (uint64_t)nb, (uint64_t)rows};
-      const uint64_t strides2[2] = {(uint64_t)kBlockBytes, (uint64_t)nb * kBlockBytes};
-      const uint32_t box2[3] = {(uint32_t)kBlockBytes, (uint32_t)S, (uint32_t)tr};
-      if (!encode_tmap_u8_3d(&map, w, dims2, strides2, box2)) return cudaErrorInvalidValue;
-    }
+  const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)rows, (uint64_t)nb};
+  const uint64_t strides[2] = {(uint64_t)nb * kBlockBytes, (uint64_t)kBlockBytes};
+  const uint32_t box[3] = {(uint32_t)kBlockBytes, (uint32_t)RB, (uint32_t)SB};
+  if (!encode_tmap_u8_3d(&map, w, dims, strides, box)) return cudaErrorInvalidValue;
+  switch (p.lpr) {
+    case 1: return launch_bl<B, 1>(map, rows, nb, p, x, residual, y, err, dev, info, s);
+    case 2: return launch_bl<B, 2>(map, rows, nb, p, x, residual, y, err, dev, info, s);
+    default: return launch_bl<B, 4>(map, rows, nb, p, x, residual, y, err, dev, info, s);
   }
-  const int n_tiles = (rows + tr - 1) / tr;
-  const int grid = n_tiles < info.sm_count ? n_tiles : info.sm_count;
-  gemv_block144_kernel<B><<<grid, kThreads, smem, s>>>(map, rows, nb, tr, ring, rows_inner, x, residual,
-                                                       y, err);
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -335,7 +382,10 @@ bool gemv_supported(int64_t cols, int batch) {
   if (batch < 1 || batch > 8) return false;
   int dev = 0;
   cudaGetDevice(&dev);
-  return pick_ring(batch, (int)(cols / kQK), device_info(dev).max_smem_optin) != 0;
+  // the largest row count needs the fewest rows per CTA; check a tall matrix
+  const Plan p = make_plan(batch, int64_t(1) << 20, (int)(cols / kQK), device_info(dev));
+  const Plan q = make_plan(batch, 1, (int)(cols / kQK), device_info(dev));
+  return p.ring != 0 && q.ring != 0;
 }
 
 cudaError_t launch_gemv_block144(const uint8_t* w, int64_t rows, int64_t cols,

@@ -147,7 +147,7 @@ int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols, const float*
   if (!w || !x || !y) return Q4K_ERR_INVALID_ARG;
   if (!aligned16(w) || !aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)))
     return Q4K_ERR_ALIGNMENT;
-  if (!gemv_supported(cols, (int)batch)) return Q4K_ERR_UNSUPPORTED;
+  if (!gemv_supported(rows, cols, (int)batch)) return Q4K_ERR_UNSUPPORTED;
   cudaError_t e = launch_gemv_block144(static_cast<const uint8_t*>(w), rows, cols, x, (int)batch,
                                        residual, y, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return Q4K_ERR_UNSUPPORTED;

@@ -34,6 +34,7 @@
 
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cstdint>
 
 namespace q4k {
@@ -117,7 +118,7 @@ __host__ __device__ inline Layout layout(int B, int nb, int ring, int part_float
 // LPR: lanes per row (1, 2 or 4); RB = 32 / LPR rows per block.
 template <int B, int LPR>
 __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
-    const __grid_constant__ CUtensorMap tmap, int rows, int nb, int rb_per_cta, int ring,
+    const __grid_constant__ CUtensorMap tmap, int rows, int nb, int rb_per_cta, int rb_pass, int ring,
     const float* __restrict__ x, const float* __restrict__ residual,
     float* __restrict__ y, int* __restrict__ err) {
   constexpr int RB = 32 / LPR;              // rows per block
@@ -130,10 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
   const int my_rb = max(0, min(rb_per_cta, n_rb - rb0));
   const int n_sj = (nb + SB - 1) / SB;      // stages per row block
   const int n_stages = my_rb * n_sj;
-  const Layout L = layout(B, nb, ring, B * rb_per_cta * nb * RB);
+  const Layout L = layout(B, nb, ring, B * rb_pass * nb * RB);
   float* xs = reinterpret_cast<float*>(smem + L.xs);
   float* xsum = reinterpret_cast<float*>(smem + L.xsum);
-  float* part = reinterpret_cast<float*>(smem + L.part);      // [B][rb][nb][RB]
+  float* part = reinterpret_cast<float*>(smem + L.part);      // [B][rb of the pass][nb][RB]
   uint8_t* stages = smem + L.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ring;
@@ -202,105 +203,114 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
   const int lq = lane % LPR;                // this lane's share of the superblock
   const int c0 = lq * CPL;                  // first chunk of the lane
   bool ok = true;
-  // units u = warp, warp + 16, ...: stage j = u / SB, superblock slot z = u % SB
-  const int n_units = n_stages * SB;
-  for (int u = warp; u < n_units; u += kConsumerWarps) {
-    const int j = u / SB, z = u - j * SB;
-    const int slot = j % ring;
-    const uint32_t phase = (uint32_t)((j / ring) & 1);
-    const int rbl = j / n_sj, sj = j - rbl * n_sj;
-    const int sb = sj * SB + z;
-    if (ok && !tc::mbar_wait_sleep(&full[slot], phase)) {
-      ok = false;
-      if (lane == 0) atomicOr(err, 2);
-    }
-    float acc[B];
+  // Row blocks are processed in passes of at most rb_pass blocks (bounded
+  // partial-sum buffer).  Within a pass, unit u = warp, warp + 16, ... lies in
+  // stage j = j0 + u / SB at superblock slot z = u % SB.
+  for (int pb = 0; pb < my_rb; pb += rb_pass) {
+    const int n_rbp = min(rb_pass, my_rb - pb);
+    const int j0 = pb * n_sj;
+    const int n_units = n_rbp * n_sj * SB;
+    for (int u = warp; u < n_units; u += kConsumerWarps) {
+      const int jl = u / SB, z = u - jl * SB;
+      const int j = j0 + jl;
+      const int slot = j % ring;
+      const uint32_t phase = (uint32_t)((j / ring) & 1);
+      const int rbl = jl / n_sj, sj = jl - rbl * n_sj;
+      const int sb = sj * SB + z;
+      if (ok && !tc::mbar_wait_sleep(&full[slot], phase)) {
+        ok = false;
+        if (lane == 0) atomicOr(err, 2);
+      }
+      float acc[B];
 #pragma unroll
-    for (int b = 0; b < B; ++b) acc[b] = 0.0f;
-    if (sb < nb) {
-      // stage laid out [SB][RB][144] (rows inner)
-      const uint8_t* p = stages + (size_t)slot * kStageBytes + ((size_t)z * RB + r_in) * kBlockBytes;
-      const uint4 hd = *reinterpret_cast<const uint4*>(p);
-      const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
-      // scales (sc) and mins (m) of sub-blocks 0..3 and 4..7, one byte each
-      const uint32_t sc03 = hd.y & 0x3F3F3F3Fu, m03 = hd.z & 0x3F3F3F3Fu;
-      const uint32_t sc47 = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-      const uint32_t m47 = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-      float scaled[B], mins[B];
+      for (int b = 0; b < B; ++b) acc[b] = 0.0f;
+      if (sb < nb) {
+        // stage laid out [SB][RB][144] (rows inner)
+        const uint8_t* p = stages + (size_t)slot * kStageBytes + ((size_t)z * RB + r_in) * kBlockBytes;
+        const uint4 hd = *reinterpret_cast<const uint4*>(p);
+        const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
+        // scales (sc) and mins (m) of sub-blocks 0..3 and 4..7, one byte each
+        const uint32_t sc03 = hd.y & 0x3F3F3F3Fu, m03 = hd.z & 0x3F3F3F3Fu;
+        const uint32_t sc47 = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+        const uint32_t m47 = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+        float scaled[B], mins[B];
 #pragma unroll
-      for (int b = 0; b < B; ++b) scaled[b] = mins[b] = 0.0f;
+        for (int b = 0; b < B; ++b) scaled[b] = mins[b] = 0.0f;
 #pragma unroll
-      for (int cc = 0; cc < CPL; ++cc) {
-        const int c = c0 + cc;
-        const uint4 q0 = *reinterpret_cast<const uint4*>(p + 16 + 32 * c);
-        const uint4 q1 = *reinterpret_cast<const uint4*>(p + 32 + 32 * c);
-        uint64_t pe[B], po[B];
+        for (int cc = 0; cc < CPL; ++cc) {
+          const int c = c0 + cc;
+          const uint4 q0 = *reinterpret_cast<const uint4*>(p + 16 + 32 * c);
+          const uint4 q1 = *reinterpret_cast<const uint4*>(p + 32 + 32 * c);
+          uint64_t pe[B], po[B];
 #pragma unroll
-        for (int b = 0; b < B; ++b) pe[b] = po[b] = 0ull;
-        const float* xc0 = xs + ((size_t)sb * 4 + c) * kRegion;
+          for (int b = 0; b < B; ++b) pe[b] = po[b] = 0ull;
+          const float* xc0 = xs + ((size_t)sb * 4 + c) * kRegion;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint4 qq = h ? q1 : q0;
-          const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
+          for (int h = 0; h < 2; ++h) {
+            const uint4 qq = h ? q1 : q0;
+            const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint64_t f0, f1, f2, f3;
-            conv_word(words[k], f0, f1, f2, f3);
+            for (int k = 0; k < 4; ++k) {
+              uint64_t f0, f1, f2, f3;
+              conv_word(words[k], f0, f1, f2, f3);
 #pragma unroll
-            for (int b = 0; b < B; ++b) {
-              const uint4* xp = reinterpret_cast<const uint4*>(xc0 + (size_t)b * nb * 4 * kRegion + 2 * (16 * h + 4 * k));
-              fma_word(f0, f1, f2, f3, xp[0], xp[1], pe[b], po[b]);
+              for (int b = 0; b < B; ++b) {
+                const uint4* xp =
+                    reinterpret_cast<const uint4*>(xc0 + (size_t)b * nb * 4 * kRegion + 2 * (16 * h + 4 * k));
+                fma_word(f0, f1, f2, f3, xp[0], xp[1], pe[b], po[b]);
+              }
             }
           }
-        }
-        // sub-blocks 2c (low nibbles) and 2c+1 (high nibbles)
-        const uint32_t scw = c < 2 ? sc03 : sc47, mw = c < 2 ? m03 : m47;
-        const int bi = 2 * (c & 1);
-        const float sc_lo = byte_f(scw, bi), sc_hi = byte_f(scw, bi + 1);
-        const float m_lo = byte_f(mw, bi), m_hi = byte_f(mw, bi + 1);
+          // sub-blocks 2c (low nibbles) and 2c+1 (high nibbles)
+          const uint32_t scw = c < 2 ? sc03 : sc47, mw = c < 2 ? m03 : m47;
+          const int bi = 2 * (c & 1);
+          const float sc_lo = byte_f(scw, bi), sc_hi = byte_f(scw, bi + 1);
+          const float m_lo = byte_f(mw, bi), m_hi = byte_f(mw, bi + 1);
 #pragma unroll
-        for (int b = 0; b < B; ++b) {
-          const float2 a = u64_as_f2(pe[b]), o = u64_as_f2(po[b]);
-          const float2 xsm = *reinterpret_cast<const float2*>(xsum + (size_t)b * nb * 8 + sb * 8 + 2 * c);
-          scaled[b] = fmaf(sc_hi, a.y + o.y, fmaf(sc_lo, a.x + o.x, scaled[b]));
-          mins[b] = fmaf(m_hi, xsm.y, fmaf(m_lo, xsm.x, mins[b]));
+          for (int b = 0; b < B; ++b) {
+            const float2 a = u64_as_f2(pe[b]), o = u64_as_f2(po[b]);
+            const float2 xsm = *reinterpret_cast<const float2*>(xsum + (size_t)b * nb * 8 + sb * 8 + 2 * c);
+            scaled[b] = fmaf(sc_hi, a.y + o.y, fmaf(sc_lo, a.x + o.x, scaled[b]));
+            mins[b] = fmaf(m_hi, xsm.y, fmaf(m_lo, xsm.x, mins[b]));
+          }
         }
+#pragma unroll
+        for (int b = 0; b < B; ++b) acc[b] = fmaf(dm.x, scaled[b], -dm.y * mins[b]);
       }
+      // release the stage once every lane of the warp has read it
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[slot]);
 #pragma unroll
-      for (int b = 0; b < B; ++b) acc[b] = fmaf(dm.x, scaled[b], -dm.y * mins[b]);
-    }
-    // release the stage once every lane of the warp has read it
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&empty[slot]);
+      for (int b = 0; b < B; ++b) {
+        if (LPR >= 2) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 1);
+        if (LPR >= 4) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 2);
+      }
+      if (lq == 0 && sb < nb) {
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-      if (LPR >= 2) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 1);
-      if (LPR >= 4) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 2);
+        for (int b = 0; b < B; ++b) part[(((size_t)b * rb_pass + rbl) * nb + sb) * RB + r_in] = acc[b];
+      }
     }
-    if (lq == 0 && sb < nb) {
-#pragma unroll
-      for (int b = 0; b < B; ++b) part[(((size_t)b * rb_per_cta + rbl) * nb + sb) * RB + r_in] = acc[b];
+    named_sync_consumers();
+    // y = sum of a row's partials in superblock order (+ residual)
+    for (int i = tid; i < B * n_rbp * RB; i += kConsumers) {
+      const int b = i / (n_rbp * RB), rem = i - b * n_rbp * RB;
+      const int rbl = rem / RB, r = rem - rbl * RB;
+      const int row = (rb0 + pb + rbl) * RB + r;
+      if (row < rows && ok) {
+        const float* pp = part + (((size_t)b * rb_pass + rbl) * nb) * RB + r;
+        float v = 0.0f;
+        for (int s2 = 0; s2 < nb; ++s2) v += pp[(size_t)s2 * RB];
+        if (residual) v += residual[(size_t)b * rows + row];
+        y[(size_t)b * rows + row] = v;
+      }
     }
-  }
-  named_sync_consumers();
-  // y = sum of a row's partials in superblock order (+ residual)
-  for (int i = tid; i < B * my_rb * RB; i += kConsumers) {
-    const int b = i / (my_rb * RB), rem = i - b * my_rb * RB;
-    const int rbl = rem / RB, r = rem - rbl * RB;
-    const int row = (rb0 + rbl) * RB + r;
-    if (row < rows && ok) {
-      const float* pp = part + (((size_t)b * rb_per_cta + rbl) * nb) * RB + r;
-      float v = 0.0f;
-      for (int s = 0; s < nb; ++s) v += pp[(size_t)s * RB];
-      if (residual) v += residual[(size_t)b * rows + row];
-      y[(size_t)b * rows + row] = v;
-    }
+    named_sync_consumers();
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 struct Plan {
-  int lpr, rb_per_cta, grid, ring;
+  int lpr, rb_per_cta, rb_pass, grid, ring;
   size_t smem;
 };
 
@@ -322,9 +332,11 @@ Plan make_plan(int B, int64_t rows, int nb, const DeviceInfo& info) {
   const int n_rb = (int)((rows + RB - 1) / RB);
   p.rb_per_cta = (n_rb + info.sm_count - 1) / info.sm_count;
   p.grid = (n_rb + p.rb_per_cta - 1) / p.rb_per_cta;
+  // partial sums of at most 16 KB per pass
+  p.rb_pass = (int)std::max<int64_t>(1, std::min<int64_t>(p.rb_per_cta, 4096 / ((int64_t)B * nb * RB)));
   p.ring = 0;
   for (int ring = kMaxRing; ring >= 2; --ring) {
-    const size_t total = layout(B, nb, ring, B * p.rb_per_cta * nb * RB).total;
+    const size_t total = layout(B, nb, ring, B * p.rb_pass * nb * RB).total;
     if (total <= (size_t)info.max_smem_optin) {
       p.ring = ring;
       p.smem = total;
@@ -347,8 +359,8 @@ cudaError_t launch_bl(const CUtensorMap& map, int rows, int nb, const Plan& p, c
     if (e != cudaSuccess) return e;
     limit = info.max_smem_optin;
   }
-  gemv_block144_kernel<B, LPR><<<p.grid, kThreads, p.smem, s>>>(map, rows, nb, p.rb_per_cta, p.ring, x,
-                                                                residual, y, err);
+  gemv_block144_kernel<B, LPR><<<p.grid, kThreads, p.smem, s>>>(map, rows, nb, p.rb_per_cta, p.rb_pass,
+                                                                p.ring, x, residual, y, err);
   return cudaGetLastError();
 }
 
@@ -378,14 +390,11 @@ cudaError_t launch_b(const uint8_t* w, int rows, int nb, const float* x,
 
 }  // namespace
 
-bool gemv_supported(int64_t cols, int batch) {
+bool gemv_supported(int64_t rows, int64_t cols, int batch) {
   if (batch < 1 || batch > 8) return false;
   int dev = 0;
   cudaGetDevice(&dev);
-  // the largest row count needs the fewest rows per CTA; check a tall matrix
-  const Plan p = make_plan(batch, int64_t(1) << 20, (int)(cols / kQK), device_info(dev));
-  const Plan q = make_plan(batch, 1, (int)(cols / kQK), device_info(dev));
-  return p.ring != 0 && q.ring != 0;
+  return make_plan(batch, rows, (int)(cols / kQK), device_info(dev)).ring != 0;
 }
 
 cudaError_t launch_gemv_block144(const uint8_t* w, int64_t rows, int64_t cols,

@@ -38,7 +38,7 @@ cudaError_t launch_gemv_block144(const uint8_t* w, int64_t rows, int64_t cols,
                                  const float* x, int batch,
                                  const float* residual, float* y,
                                  cudaStream_t s);
-bool gemv_supported(int64_t cols, int batch);
+bool gemv_supported(int64_t rows, int64_t cols, int batch);
 
 // Small-tile integer MMQ on CUDA cores (dp4a).  When `p_out` is non-null
 // the kernel stores the raw per-block integer dots there instead of y.

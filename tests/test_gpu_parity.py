@@ -94,6 +94,18 @@ def test_gemv_parity(rows, cols, batch, res):
     assert_close(y, y_ref, norm, f"gemv {rows}x{cols} b{batch}")
 
 
+def test_gemv_tall_matrix_sampled_rows():
+    # many row blocks per SM and a long K: the kernel reduces in several passes
+    rows, cols = 20000, 12288
+    f = synth.q4k_fields(rows, cols, 4242)
+    x = synth.activations(2, cols, 4243)
+    y = run_gemv(f, x)
+    rng = np.random.default_rng(9)
+    sample = np.sort(rng.choice(rows, 384, replace=False))
+    y_ref, norm = O.gemv(slice_rows(f, sample), x)
+    assert_close(y[:, sample], y_ref, norm, "20000x12288 sampled")
+
+
 def test_gemv_single_2048_seed0():
     f, x = synth.single_gemv_2048(0)
     y = run_gemv(f, x)

@@ -104,6 +104,19 @@ int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols,
              void* stream);
 
 /*
+ * q4k_gemv_multi - one decode GEMV launch over n (1..4) matrices that share
+ * the input x (genie-ai-runtime §4, Path C: one kernel for the QKV triple and
+ * for the gate/up pair).  w, rows, y (and residual, if not NULL) are HOST
+ * arrays of n entries; entry m is a q4k_gemv problem with its own device
+ * pointers w[m], y[m], residual[m] (nullable) and row count rows[m].  All
+ * matrices have `cols` inputs.  Matrices with rows[m] == 0 are skipped.
+ * Same accuracy and determinism as q4k_gemv; n > 4 gives Q4K_ERR_UNSUPPORTED.
+ */
+int q4k_gemv_multi(int n, const void* const* w, int layout, const int64_t* rows,
+                   int64_t cols, const float* x, int64_t batch,
+                   const float* const* residual, float* const* y, void* stream);
+
+/*
  * q4k_gemm - prefill MMQ GEMM (genie-ai-runtime §3, "The tensor-core kernel
  * (Path E)"; integer form over q8_1 activations):
  *   y[t][o] = sum_b ( d*sc[o,b] * d8[t,b] * P[t,o,b]

@@ -31,6 +31,7 @@ SIGNATURES = {
     "q4k_pack": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _P, _P]),
     "q8_quantize": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q4k_gemv": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "q4k_gemv_multi": (_I, [_I, _P, _I, _P, _I64, _P, _I64, _P, _P, _P]),
     "q4k_gemm": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
     "q4k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
     "q4k_device_error": (_I, [_P]),
@@ -140,6 +141,23 @@ def q4k_gemv(w, rows: int, cols: int, x, residual=None, y=None, layout: int = BL
     return y
 
 
+def q4k_gemv_multi(ws, rows, cols: int, x, residuals=None, ys=None, layout: int = BLOCK144, stream=None):
+    """One launch of several GEMVs sharing ``x``: ``ys[m] = W_m x (+ residuals[m])``."""
+    n = len(ws)
+    batch = x.shape[0]
+    if ys is None:
+        ys = [torch.empty((batch, r), dtype=torch.float32, device=x.device) for r in rows]
+    wp = (ctypes.c_void_p * n)(*[_ptr(w, torch.uint8, "w") for w in ws])
+    rp = (ctypes.c_int64 * n)(*[int(r) for r in rows])
+    yp = (ctypes.c_void_p * n)(*[_ptr(y, torch.float32, "y") for y in ys])
+    resp = None
+    if residuals is not None:
+        resp = (ctypes.c_void_p * n)(*[_ptr(r, torch.float32, "residual") for r in residuals])
+    _check(lib().q4k_gemv_multi(n, wp, layout, rp, cols, _ptr(x, torch.float32, "x"), batch,
+                                resp, yp, _stream(stream)), "q4k_gemv_multi")
+    return ys
+
+
 def q4k_gemm(w, rows: int, cols: int, q8, d8, s, y=None, layout: int = BLOCK144, stream=None):
     """Prefill MMQ GEMM on q8_1 activations; returns ``y`` [tokens][rows] float32."""
     tokens = q8.shape[0]
@@ -174,5 +192,5 @@ def q4k_version() -> str:
 
 
 __all__ = ["build", "lib", "Q4KError", "BLOCK144", "q4k_packed_bytes", "q4k_pack", "q8_quantize",
-           "q4k_gemv", "q4k_gemm", "q4k_gemm_blockdots", "q4k_device_error", "q4k_version",
+           "q4k_gemv", "q4k_gemv_multi", "q4k_gemm", "q4k_gemm_blockdots", "q4k_device_error", "q4k_version",
            "SIGNATURES"]

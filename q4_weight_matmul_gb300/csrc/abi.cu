@@ -137,6 +137,42 @@ int q8_quantize(const float* x, int64_t tokens, int64_t cols, int8_t* q, float* 
   return e == cudaSuccess ? Q4K_OK : record_cuda(e);
 }
 
+int q4k_gemv_multi(int n, const void* const* w, int layout, const int64_t* rows, int64_t cols,
+                   const float* x, int64_t batch, const float* const* residual, float* const* y,
+                   void* stream) {
+  if (n < 1 || n > gemv_max_mats()) return n < 1 ? Q4K_ERR_INVALID_ARG : Q4K_ERR_UNSUPPORTED;
+  if (!w || !rows || !y) return Q4K_ERR_INVALID_ARG;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_layout(layout)) return e;
+  if (batch < 0 || batch > 8) return batch < 0 ? Q4K_ERR_INVALID_ARG : Q4K_ERR_UNSUPPORTED;
+  // drop empty matrices; nothing to do if all are empty
+  const uint8_t* wk[8];
+  int64_t rk[8];
+  const float* resk[8];
+  float* yk[8];
+  int k = 0;
+  for (int m = 0; m < n; ++m) {
+    if (int e = check_rows(rows[m])) return e;
+    if (rows[m] == 0) continue;
+    if (!w[m] || !y[m]) return Q4K_ERR_INVALID_ARG;
+    const float* r = residual ? residual[m] : nullptr;
+    if (!aligned16(w[m]) || !aligned16(y[m]) || (r && !aligned16(r))) return Q4K_ERR_ALIGNMENT;
+    wk[k] = static_cast<const uint8_t*>(w[m]);
+    rk[k] = rows[m];
+    resk[k] = r;
+    yk[k] = y[m];
+    ++k;
+  }
+  if (k == 0 || batch == 0) return Q4K_OK;
+  if (!x) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(x)) return Q4K_ERR_ALIGNMENT;
+  if (!gemv_supported(rk, k, cols, (int)batch)) return Q4K_ERR_UNSUPPORTED;
+  cudaError_t e = launch_gemv_block144(wk, rk, k, cols, x, (int)batch, resk, yk,
+                                       static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return Q4K_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
 int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols, const float* x,
              int64_t batch, const float* residual, float* y, void* stream) {
   if (int e = check_rows(rows)) return e;
@@ -145,13 +181,9 @@ int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols, const float*
   if (batch < 0 || batch > 8) return batch < 0 ? Q4K_ERR_INVALID_ARG : Q4K_ERR_UNSUPPORTED;
   if (rows == 0 || batch == 0) return Q4K_OK;
   if (!w || !x || !y) return Q4K_ERR_INVALID_ARG;
-  if (!aligned16(w) || !aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)))
-    return Q4K_ERR_ALIGNMENT;
-  if (!gemv_supported(rows, cols, (int)batch)) return Q4K_ERR_UNSUPPORTED;
-  cudaError_t e = launch_gemv_block144(static_cast<const uint8_t*>(w), rows, cols, x, (int)batch,
-                                       residual, y, static_cast<cudaStream_t>(stream));
-  if (e == cudaErrorNotSupported) return Q4K_ERR_UNSUPPORTED;
-  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+  const float* const res[1] = {residual};
+  float* const ys[1] = {y};
+  return q4k_gemv_multi(1, &w, layout, &rows, cols, x, batch, res, ys, stream);
 }
 
 static int gemm_common(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8,

@@ -1,25 +1,31 @@
-// q4k_gemv: decode GEMV y[b][o] = sum_k w[o][k] x[b][k] (+ residual) over
-// BLOCK144 Q4_K weights (genie-ai-runtime §4, Path C: packed quants read as
-// whole words, dequantised in registers, residual folded in).
+// q4k_gemv / q4k_gemv_multi: decode GEMV y[b][o] = sum_k w[o][k] x[b][k]
+// (+ residual) over BLOCK144 Q4_K weights (genie-ai-runtime §4, Path C: packed
+// quants read as whole words, dequantised in registers, residual folded in,
+// and one kernel for matrices that share their input: the QKV triple and the
+// gate/up pair).
 //
-// Work split.  Rows are cut into blocks of RB rows (RB = 32, 16 or 8, the
-// largest that still gives every SM a block); one CTA per SM owns a run of
-// row blocks and all their superblocks.  A unit of work is one row block x
-// one superblock; the 16 consumer warps of a CTA take units round-robin, so
-// every warp streams several superblocks and K is split across warps.  Each
-// unit leaves one partial sum per row in shared memory; at the end the CTA
-// adds a row's partials in superblock order (bitwise deterministic).
+// Work split.  Rows are cut into blocks of RB rows (RB = 32, 16 or 8, chosen
+// so that the busiest SM holds the fewest rows); one CTA per SM owns a run of
+// row blocks (of one or several matrices) and all their superblocks.  A unit
+// of work is one row block x one superblock; the 16 consumer warps take units
+// round-robin, so K is split across warps.  Each unit leaves one partial sum
+// per row in shared memory and the CTA adds a row's partials in superblock
+// order (bitwise deterministic).
 //
-// Streaming.  A producer warp fetches the CTA's weights with 3-D tensor
-// copies: one copy per stage of RB rows x (128/RB) superblocks (18 KB, out of
-// range rows and superblocks zero-filled) into a ring of stages.  It starts
-// at launch, before the activations are staged, so bytes in flight are set by
-// the ring, not by registers.
+// Streaming.  A producer warp fetches the weights with 3-D tensor copies:
+// one copy per stage of RB rows x (128/RB) superblocks (18 KB, out-of-range
+// rows and superblocks zero-filled) into a ring of stages.  The copies start
+// at launch, before the activations are read.  Kernels are launched as
+// programmatic dependents and a CTA stays under half of an SM (<= 60
+// registers per thread, <= ~110 KB of shared memory), so the next GEMV's CTA
+// can sit beside this one and stream its weights while this one finishes;
+// griddepcontrol.wait still orders every activation read after the previous
+// kernel has completed.
 //
 // Lanes.  32/RB lanes share a row: with RB = 32 a lane owns a row's whole
 // superblock (256 weights), with RB = 16 half of it, with RB = 8 one 64-weight
 // chunk.  A chunk's 32 quant bytes hold sub-block 2c in low nibbles and 2c+1
-// in high nibbles, so scale/min decoding is paid once per 64-256 weights.
+// in high nibbles.
 //
 // Dequantisation.  A nibble at bit position p (p <= 16) ORed into the float
 // 2^23 gives 2^23 + q*2^p exactly; subtracting 2^23 leaves q*2^p, and the
@@ -36,6 +42,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstring>
 
 namespace q4k {
 namespace {
@@ -46,15 +53,21 @@ constexpr int kThreads = kConsumers + 32;     // + one producer warp
 constexpr int kRegion = 68;                   // floats per (token, superblock, chunk): 32 (lo,hi) pairs + pad
 constexpr int kStageSuper = 128;              // superblock-rows per stage (RB * SB)
 constexpr int kStageBytes = kStageSuper * kBlockBytes;
-constexpr int kMaxRing = 8;
+constexpr int kMaxRing = 6;
+constexpr size_t kPairSmem = 110 * 1024;      // a CTA this small leaves room for a neighbour
+constexpr int kMaxMats = 4;
 
-// Power-of-two pre-scale exponent of weight l (0..31) of the low (hi = 0) or
-// high (hi = 1) half of a chunk; matches the nibble positions used below.
-__device__ __forceinline__ int nib_shift(int l, int hi) {
-  const uint32_t lo_tab = 0u | (8u << 8) | (16u << 16) | (12u << 24);
-  const uint32_t hi_tab = 4u | (12u << 8) | (8u << 16) | (16u << 24);
-  return (int)(((hi ? hi_tab : lo_tab) >> (8 * (l & 3))) & 0xFFu);
-}
+struct GemvParams {
+  CUtensorMap map[kMaxMats];
+  float* y[kMaxMats];
+  const float* res[kMaxMats];
+  int rows[kMaxMats];
+  int rb_start[kMaxMats + 1];   // prefix sums of row blocks per matrix
+  int n_mats;
+  int nb, rb_per_cta, rb_pass, ring;
+  const float* x;
+  int* err;
+};
 
 __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
@@ -115,20 +128,74 @@ __host__ __device__ inline Layout layout(int B, int nb, int ring, int part_float
   return L;
 }
 
+// which matrix a global row block belongs to
+__device__ __forceinline__ int mat_of(const GemvParams& P, int g) {
+  int m = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxMats; ++i)
+    if (i < P.n_mats && g >= P.rb_start[i]) m = i;
+  return m;
+}
+
+// Activations staged once: pre-scaled by 2^-p, (lo, hi)-paired per chunk, and
+// summed over each 32-wide sub-block.  All loads of a round are issued before
+// any use; eight lanes hold one sub-block, so its sum is three shuffles.
+template <int B>
+__device__ __forceinline__ void stage_x(const float* __restrict__ x, int nb, float* xs, float* xsum,
+                                        int tid) {
+  const int row4 = nb * 64;                     // float4 per activation row
+  const int n4 = B * row4;                      // a multiple of 64: whole warps
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  for (int base = tid; base < n4; base += 4 * kConsumers) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * kConsumers;
+      if (idx < n4) v[u] = __ldg(x4 + idx);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * kConsumers;
+      if (idx < n4) {
+        const int b = idx / row4, k = 4 * (idx - b * row4);
+        const int s = k >> 8, r = k & 255, c = r >> 6, t = r & 63;
+        const int hi = t >> 5, l = t & 31;
+        float* dst = xs + (((size_t)b * nb + s) * 4 + c) * kRegion + 2 * l + hi;
+        // scale exponents of l%4 = 0..3: low half 0, 8, 16, 12; high half 4, 12, 8, 16
+        if (hi) {
+          dst[0] = v[u].x * 0x1p-4f;
+          dst[2] = v[u].y * 0x1p-12f;
+          dst[4] = v[u].z * 0x1p-8f;
+          dst[6] = v[u].w * 0x1p-16f;
+        } else {
+          dst[0] = v[u].x;
+          dst[2] = v[u].y * 0x1p-8f;
+          dst[4] = v[u].z * 0x1p-16f;
+          dst[6] = v[u].w * 0x1p-12f;
+        }
+        float sum = (v[u].x + v[u].y) + (v[u].z + v[u].w);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        if ((idx & 7) == 0) xsum[(size_t)b * nb * 8 + (k >> 5)] = sum;
+      }
+    }
+  }
+}
+
 // LPR: lanes per row (1, 2 or 4); RB = 32 / LPR rows per block.
 template <int B, int LPR>
-__global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
-    const __grid_constant__ CUtensorMap tmap, int rows, int nb, int rb_per_cta, int rb_pass, int ring,
-    const float* __restrict__ x, const float* __restrict__ residual,
-    float* __restrict__ y, int* __restrict__ err) {
+__global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kernel(
+    const __grid_constant__ GemvParams P) {
   constexpr int RB = 32 / LPR;              // rows per block
   constexpr int SB = kStageSuper / RB;      // superblocks per stage
   constexpr int CPL = 4 / LPR;              // 64-weight chunks per lane
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int n_rb = (rows + RB - 1) / RB;
-  const int rb0 = blockIdx.x * rb_per_cta;
-  const int my_rb = max(0, min(rb_per_cta, n_rb - rb0));
+  const int nb = P.nb, ring = P.ring, rb_pass = P.rb_pass;
+  const int n_rb = P.rb_start[P.n_mats];
+  const int rb0 = blockIdx.x * P.rb_per_cta;
+  const int my_rb = max(0, min(P.rb_per_cta, n_rb - rb0));
   const int n_sj = (nb + SB - 1) / SB;      // stages per row block
   const int n_stages = my_rb * n_sj;
   const Layout L = layout(B, nb, ring, B * rb_pass * nb * RB);
@@ -138,11 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
   uint8_t* stages = smem + L.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ring;
-
-  const int cols = nb * kQK;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
+  // the next kernel in the stream may start its own weight stream now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < ring; ++i) {
       tc::mbar_init(&full[i], 1);
@@ -155,19 +222,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap) : "memory");
-      int slot = 0, rb = 0, sj = 0;
+      int slot = 0, g = rb0, sj = 0;
+      int m = mat_of(P, g);
       uint32_t phase = 0;
       for (int j = 0; j < n_stages; ++j) {
         if (!tc::mbar_wait_sleep(&empty[slot], phase ^ 1)) {
-          atomicOr(err, 2);
+          atomicOr(P.err, 2);
           break;
         }
         tc::mbar_arrive_expect_tx(&full[slot], kStageBytes);
-        tc::tma_load_3d(stages + (size_t)slot * kStageBytes, &tmap, 0, (rb0 + rb) * RB, sj * SB, &full[slot]);
+        tc::tma_load_3d(stages + (size_t)slot * kStageBytes, &P.map[m], 0, (g - P.rb_start[m]) * RB, sj * SB,
+                        &full[slot]);
         if (++sj == n_sj) {
           sj = 0;
-          ++rb;
+          ++g;
+          m = mat_of(P, g);
         }
         if (++slot == ring) {
           slot = 0;
@@ -180,23 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
 
   // -------------------------------------------------------------- consumers
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (int i = tid; i < B * cols; i += kConsumers) {
-    const int b = i / cols, k = i - b * cols;
-    const int s = k >> 8, r = k & 255, cc = r >> 6, t = r & 63;
-    const int hi = t >> 5, l = t & 31;
-    const float scale = __uint_as_float((uint32_t)(127 - nib_shift(l, hi)) << 23);
-    xs[(((size_t)b * nb + s) * 4 + cc) * kRegion + 2 * l + hi] = x[(size_t)b * cols + k] * scale;
-  }
-  for (int i = warp; i < B * nb * 2; i += kConsumerWarps) {
-    const int sbk = 4 * i + (lane >> 3);
-    const int b = sbk / (nb * 8), j = sbk - b * nb * 8;
-    const float4 v = *reinterpret_cast<const float4*>(x + (size_t)b * cols + 32 * j + 4 * (lane & 7));
-    float sum = (v.x + v.y) + (v.z + v.w);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-    if ((lane & 7) == 0) xsum[sbk] = sum;
-  }
+  stage_x<B>(P.x, nb, xs, xsum, tid);
   named_sync_consumers();
 
   const int r_in = lane / LPR;              // row inside the block
@@ -219,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
       const int sb = sj * SB + z;
       if (ok && !tc::mbar_wait_sleep(&full[slot], phase)) {
         ok = false;
-        if (lane == 0) atomicOr(err, 2);
+        if (lane == 0) atomicOr(P.err, 2);
       }
       float acc[B];
 #pragma unroll
@@ -295,18 +348,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
     for (int i = tid; i < B * n_rbp * RB; i += kConsumers) {
       const int b = i / (n_rbp * RB), rem = i - b * n_rbp * RB;
       const int rbl = rem / RB, r = rem - rbl * RB;
-      const int row = (rb0 + pb + rbl) * RB + r;
+      const int g = rb0 + pb + rbl;
+      const int m = mat_of(P, g);
+      const int rows = P.rows[m];
+      const int row = (g - P.rb_start[m]) * RB + r;
       if (row < rows && ok) {
         const float* pp = part + (((size_t)b * rb_pass + rbl) * nb) * RB + r;
         float v = 0.0f;
         for (int s2 = 0; s2 < nb; ++s2) v += pp[(size_t)s2 * RB];
-        if (residual) v += residual[(size_t)b * rows + row];
-        y[(size_t)b * rows + row] = v;
+        if (P.res[m]) v += P.res[m][(size_t)b * rows + row];
+        P.y[m][(size_t)b * rows + row] = v;
       }
     }
     named_sync_consumers();
   }
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 struct Plan {
@@ -314,14 +369,16 @@ struct Plan {
   size_t smem;
 };
 
-Plan make_plan(int B, int64_t rows, int nb, const DeviceInfo& info) {
+Plan make_plan(int B, const int64_t* rows, int n_mats, int nb, const DeviceInfo& info) {
   Plan p{};
   // rows per block: the one whose busiest SM holds the fewest rows (ties go to
   // the taller block, which decodes scales less often)
   p.lpr = 4;
   int64_t best = INT64_MAX;
   for (int lpr = 1; lpr <= 4; lpr *= 2) {
-    const int64_t rb = 32 / lpr, n_rb = (rows + rb - 1) / rb;
+    const int64_t rb = 32 / lpr;
+    int64_t n_rb = 0;
+    for (int m = 0; m < n_mats; ++m) n_rb += (rows[m] + rb - 1) / rb;
     const int64_t per = (n_rb + info.sm_count - 1) / info.sm_count;
     if (per * rb < best) {
       best = per * rb;
@@ -329,26 +386,31 @@ Plan make_plan(int B, int64_t rows, int nb, const DeviceInfo& info) {
     }
   }
   const int RB = 32 / p.lpr;
-  const int n_rb = (int)((rows + RB - 1) / RB);
-  p.rb_per_cta = (n_rb + info.sm_count - 1) / info.sm_count;
-  p.grid = (n_rb + p.rb_per_cta - 1) / p.rb_per_cta;
-  // partial sums of at most 16 KB per pass
-  p.rb_pass = (int)std::max<int64_t>(1, std::min<int64_t>(p.rb_per_cta, 4096 / ((int64_t)B * nb * RB)));
+  int64_t n_rb = 0;
+  for (int m = 0; m < n_mats; ++m) n_rb += (rows[m] + RB - 1) / RB;
+  p.rb_per_cta = (int)((n_rb + info.sm_count - 1) / info.sm_count);
+  p.grid = (int)((n_rb + p.rb_per_cta - 1) / p.rb_per_cta);
+  // partial sums of at most 8 KB per pass
+  p.rb_pass = (int)std::max<int64_t>(1, std::min<int64_t>(p.rb_per_cta, 2048 / ((int64_t)B * nb * RB)));
+  // the deepest ring that keeps the CTA small enough to pair with the next
+  // kernel's; failing that, the deepest ring that fits at all
   p.ring = 0;
-  for (int ring = kMaxRing; ring >= 2; --ring) {
-    const size_t total = layout(B, nb, ring, B * p.rb_pass * nb * RB).total;
-    if (total <= (size_t)info.max_smem_optin) {
-      p.ring = ring;
-      p.smem = total;
-      break;
+  const size_t caps[2] = {kPairSmem, (size_t)info.max_smem_optin};
+  for (size_t cap : caps) {
+    for (int ring = kMaxRing; ring >= 2 && p.ring == 0; --ring) {
+      const size_t total = layout(B, nb, ring, B * p.rb_pass * nb * RB).total;
+      if (total <= cap) {
+        p.ring = ring;
+        p.smem = total;
+      }
     }
+    if (p.ring) break;
   }
   return p;
 }
 
 template <int B, int LPR>
-cudaError_t launch_bl(const CUtensorMap& map, int rows, int nb, const Plan& p, const float* x,
-                      const float* residual, float* y, int* err, int dev, const DeviceInfo& info,
+cudaError_t launch_bl(const GemvParams& params, const Plan& p, int dev, const DeviceInfo& info,
                       cudaStream_t s) {
   static int s_limit[64];
   int& limit = s_limit[dev & 63];
@@ -359,59 +421,82 @@ cudaError_t launch_bl(const CUtensorMap& map, int rows, int nb, const Plan& p, c
     if (e != cudaSuccess) return e;
     limit = info.max_smem_optin;
   }
-  gemv_block144_kernel<B, LPR><<<p.grid, kThreads, p.smem, s>>>(map, rows, nb, p.rb_per_cta, p.rb_pass,
-                                                                p.ring, x, residual, y, err);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_block144_kernel<B, LPR>, params);
 }
 
 template <int B>
-cudaError_t launch_b(const uint8_t* w, int rows, int nb, const float* x,
-                     const float* residual, float* y, cudaStream_t s) {
+cudaError_t launch_b(const uint8_t* const* w, const int64_t* rows, int n_mats, int nb, const float* x,
+                     const float* const* residual, float* const* y, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   const DeviceInfo& info = device_info(dev);
-  const Plan p = make_plan(B, rows, nb, info);
+  const Plan p = make_plan(B, rows, n_mats, nb, info);
   if (p.ring == 0) return cudaErrorNotSupported;
-  int* err = device_error_word();
-  if (!err) return cudaErrorInvalidValue;
+  GemvParams params;
+  memset(&params, 0, sizeof(params));
+  params.err = device_error_word();
+  if (!params.err) return cudaErrorInvalidValue;
   const int RB = 32 / p.lpr, SB = kStageSuper / RB;
-  // box: bytes of a superblock x RB rows x SB superblocks, rows inner in shared memory
-  CUtensorMap map;
-  const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)rows, (uint64_t)nb};
-  const uint64_t strides[2] = {(uint64_t)nb * kBlockBytes, (uint64_t)kBlockBytes};
-  const uint32_t box[3] = {(uint32_t)kBlockBytes, (uint32_t)RB, (uint32_t)SB};
-  if (!encode_tmap_u8_3d(&map, w, dims, strides, box)) return cudaErrorInvalidValue;
+  params.n_mats = n_mats;
+  params.rb_start[0] = 0;
+  for (int m = 0; m < n_mats; ++m) {
+    // box: a superblock's bytes x RB rows x SB superblocks, rows inner in shared memory
+    const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)rows[m], (uint64_t)nb};
+    const uint64_t strides[2] = {(uint64_t)nb * kBlockBytes, (uint64_t)kBlockBytes};
+    const uint32_t box[3] = {(uint32_t)kBlockBytes, (uint32_t)RB, (uint32_t)SB};
+    if (!encode_tmap_u8_3d(&params.map[m], w[m], dims, strides, box)) return cudaErrorInvalidValue;
+    params.y[m] = y[m];
+    params.res[m] = residual ? residual[m] : nullptr;
+    params.rows[m] = (int)rows[m];
+    params.rb_start[m + 1] = params.rb_start[m] + (int)((rows[m] + RB - 1) / RB);
+  }
+  for (int m = n_mats; m < kMaxMats; ++m) params.rb_start[m + 1] = params.rb_start[m];
+  params.nb = nb;
+  params.rb_per_cta = p.rb_per_cta;
+  params.rb_pass = p.rb_pass;
+  params.ring = p.ring;
+  params.x = x;
   switch (p.lpr) {
-    case 1: return launch_bl<B, 1>(map, rows, nb, p, x, residual, y, err, dev, info, s);
-    case 2: return launch_bl<B, 2>(map, rows, nb, p, x, residual, y, err, dev, info, s);
-    default: return launch_bl<B, 4>(map, rows, nb, p, x, residual, y, err, dev, info, s);
+    case 1: return launch_bl<B, 1>(params, p, dev, info, s);
+    case 2: return launch_bl<B, 2>(params, p, dev, info, s);
+    default: return launch_bl<B, 4>(params, p, dev, info, s);
   }
 }
 
 }  // namespace
 
-bool gemv_supported(int64_t rows, int64_t cols, int batch) {
-  if (batch < 1 || batch > 8) return false;
+int gemv_max_mats() { return kMaxMats; }
+
+bool gemv_supported(const int64_t* rows, int n_mats, int64_t cols, int batch) {
+  if (batch < 1 || batch > 8 || n_mats < 1 || n_mats > kMaxMats) return false;
   int dev = 0;
   cudaGetDevice(&dev);
-  return make_plan(batch, rows, (int)(cols / kQK), device_info(dev)).ring != 0;
+  return make_plan(batch, rows, n_mats, (int)(cols / kQK), device_info(dev)).ring != 0;
 }
 
-cudaError_t launch_gemv_block144(const uint8_t* w, int64_t rows, int64_t cols,
-                                 const float* x, int batch,
-                                 const float* residual, float* y,
-                                 cudaStream_t s) {
-  if (rows == 0 || batch == 0) return cudaSuccess;
+cudaError_t launch_gemv_block144(const uint8_t* const* w, const int64_t* rows, int n_mats, int64_t cols,
+                                 const float* x, int batch, const float* const* residual,
+                                 float* const* y, cudaStream_t s) {
   const int nb = (int)(cols / kQK);
   switch (batch) {
-    case 1: return launch_b<1>(w, (int)rows, nb, x, residual, y, s);
-    case 2: return launch_b<2>(w, (int)rows, nb, x, residual, y, s);
-    case 3: return launch_b<3>(w, (int)rows, nb, x, residual, y, s);
-    case 4: return launch_b<4>(w, (int)rows, nb, x, residual, y, s);
-    case 5: return launch_b<5>(w, (int)rows, nb, x, residual, y, s);
-    case 6: return launch_b<6>(w, (int)rows, nb, x, residual, y, s);
-    case 7: return launch_b<7>(w, (int)rows, nb, x, residual, y, s);
-    case 8: return launch_b<8>(w, (int)rows, nb, x, residual, y, s);
+    case 1: return launch_b<1>(w, rows, n_mats, nb, x, residual, y, s);
+    case 2: return launch_b<2>(w, rows, n_mats, nb, x, residual, y, s);
+    case 3: return launch_b<3>(w, rows, n_mats, nb, x, residual, y, s);
+    case 4: return launch_b<4>(w, rows, n_mats, nb, x, residual, y, s);
+    case 5: return launch_b<5>(w, rows, n_mats, nb, x, residual, y, s);
+    case 6: return launch_b<6>(w, rows, n_mats, nb, x, residual, y, s);
+    case 7: return launch_b<7>(w, rows, n_mats, nb, x, residual, y, s);
+    case 8: return launch_b<8>(w, rows, n_mats, nb, x, residual, y, s);
     default: return cudaErrorNotSupported;
   }
 }

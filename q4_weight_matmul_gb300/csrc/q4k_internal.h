@@ -32,13 +32,15 @@ cudaError_t launch_q8_quantize(const float* x, int64_t tokens, int64_t cols,
                                int8_t* q, float* d8, int32_t* sum,
                                cudaStream_t s);
 
-// Returns cudaErrorNotSupported when (batch, cols) does not fit the kernel's
+// Decode GEMV over n_mats (1..gemv_max_mats()) matrices that share one input
+// x; matrix m has rows[m] rows, output y[m] and optional residual[m].
+// Returns cudaErrorNotSupported when the shape does not fit the kernel's
 // shared-memory staging of the activations.
-cudaError_t launch_gemv_block144(const uint8_t* w, int64_t rows, int64_t cols,
-                                 const float* x, int batch,
-                                 const float* residual, float* y,
-                                 cudaStream_t s);
-bool gemv_supported(int64_t rows, int64_t cols, int batch);
+int gemv_max_mats();
+cudaError_t launch_gemv_block144(const uint8_t* const* w, const int64_t* rows, int n_mats, int64_t cols,
+                                 const float* x, int batch, const float* const* residual,
+                                 float* const* y, cudaStream_t s);
+bool gemv_supported(const int64_t* rows, int n_mats, int64_t cols, int batch);
 
 // Small-tile integer MMQ on CUDA cores (dp4a).  When `p_out` is non-null
 // the kernel stores the raw per-block integer dots there instead of y.

@@ -122,6 +122,38 @@ def test_gemv_qwen3_4b_decode_set(batch):
         assert_close(y, y_ref, norm, name)
 
 
+@pytest.mark.parametrize("batch", [1, 2])
+def test_gemv_multi_qkv_and_gate_up(batch):
+    fields, xs = synth.decode_layer(synth.WL_DECODE_4B, 1, batch)
+    for names, inp in ((("q", "k", "v"), "attn_in"), (("gate", "up"), "mlp_in")):
+        shapes = {n: (r, c) for n, r, c, _ in synth.QWEN3_4B_LAYER}
+        cols = shapes[names[0]][1]
+        ws = [pack_dev(fields[n]) for n in names]
+        x = torch.from_numpy(xs[inp]).cuda()
+        res = [torch.from_numpy(synth.residual(batch, shapes[n][0], [5, i])).cuda() for i, n in enumerate(names)]
+        ys = q4k.q4k_gemv_multi(ws, [shapes[n][0] for n in names], cols, x, residuals=res)
+        torch.cuda.synchronize()
+        for n, y, r in zip(names, ys, res):
+            y_ref, norm = O.gemv(fields[n], xs[inp], r.cpu().numpy())
+            assert_close(y.cpu().numpy(), y_ref, norm, f"multi {n}")
+            # the fused launch gives the same bits as the single-matrix call
+            single = q4k.q4k_gemv(ws[names.index(n)], shapes[n][0], cols, x, residual=r)
+            assert torch.equal(single, y)
+
+
+def test_gemv_multi_skips_empty_and_rejects_too_many():
+    f = synth.q4k_fields(40, 512, 3)
+    w = pack_dev(f)
+    x = torch.from_numpy(synth.activations(1, 512, 4)).cuda()
+    empty = torch.empty(0, dtype=torch.uint8, device="cuda")
+    ys = q4k.q4k_gemv_multi([w, w], [40, 0], 512, x,
+                            ys=[torch.empty((1, 40), device="cuda"), torch.empty((1, 0), device="cuda")])
+    y_ref, norm = O.gemv(f, synth.activations(1, 512, 4))
+    assert_close(host(ys[0]), y_ref, norm, "multi with an empty matrix")
+    with pytest.raises(q4k.Q4KError):
+        q4k.q4k_gemv_multi([w] * 5, [40] * 5, 512, x)
+
+
 def test_gemv_is_deterministic():
     f = synth.q4k_fields(2560, 9728, 5)
     x = synth.activations(1, 9728, 6)

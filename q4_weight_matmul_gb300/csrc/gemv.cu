@@ -191,8 +191,10 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
   constexpr int RB = 32 / LPR;              // rows per block
   constexpr int SB = kStageSuper / RB;      // superblocks per stage
   constexpr int CPL = 4 / LPR;              // 64-weight chunks per lane
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base, derived from the shared array itself so that the
+  // compiler keeps every access below in the shared state space
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int nb = P.nb, ring = P.ring, rb_pass = P.rb_pass;
   const int n_rb = P.rb_start[P.n_mats];
   const int rb0 = blockIdx.x * P.rb_per_cta;

@@ -9,17 +9,14 @@
 namespace q4k {
 namespace tc {
 
-// A bounded wait gives up after this many nanoseconds of wall time.
-constexpr uint64_t kTimeoutNs = 2000000000ull;
+// A bounded wait gives up after this many SM clock cycles (about 2 s at the
+// 2.07 GHz maximum clock, longer at lower clocks).  The SM cycle counter is
+// used rather than the global nanosecond timer: reading the latter takes
+// thousands of cycles, which a wait on the critical path cannot afford.
+constexpr long long kTimeoutCycles = 4000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ----------------------------------------------------------------- mbarrier
@@ -44,14 +41,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait until the phase with `parity` has completed.  Returns false (and
 // leaves the barrier alone) if `abort` becomes non-zero or the wait exceeds
-// kTimeoutNs; the caller then records the error and unwinds.
+// kTimeoutCycles; the caller then records the error and unwinds.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_ns() - t0 > kTimeoutNs) return false;
+    if (clock64() - t0 > kTimeoutCycles) return false;
   }
 }
 
@@ -91,13 +88,13 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
   return ok != 0;
 }
 
-// Bounded wait without an abort flag; sleeps between polls.
+// Bounded wait without an abort flag.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  const long long t0 = clock64();
   for (;;) {
-    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
-    if (global_ns() - t0 > kTimeoutNs) return false;
+    if (mbar_try_wait_hint(bar, parity, 1000u)) return true;
+    if (clock64() - t0 > kTimeoutCycles) return false;
   }
 }
 
@@ -140,6 +137,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
         "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns (the x16 form of tmem_ld32).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+        "r"(r[14]), "r"(r[15])
       : "memory");
 }
 

@@ -283,44 +283,66 @@ def run_ours(args, rank, world):
             else:
                 q4k.q4k_gemv_multi([layer[n] for n in names], rows, cols, xs[inp], ys=[ys[n] for n in names])
 
-    # One CUDA graph per layer copy: a replay issues the step's seven GEMV
-    # launches with no host work between them.
+    # The timed region is one CUDA graph holding exactly `steps` layer steps
+    # (rotating over the layer copies), as a decode engine replays one graph
+    # per token: no host work or graph-launch gap between steps.
     for i in range(args.warmup):
         decode_step(i)
     torch.cuda.synchronize()
-    graphs = []
-    for c in range(n_copies):
+
+    def capture(first, count):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            decode_step(c)
-        graphs.append(g)
-    for i in range(args.warmup):
-        graphs[i % n_copies].replay()
+            for i in range(first, first + count):
+                decode_step(i)
+        return g
+
+    warm_graph = capture(0, args.warmup)
+    timed_graph = capture(args.warmup, args.steps)
+    warm_graph.replay()
     sampler = ClockSampler(uuid)
     sampler.start()
     time.sleep(0.3)
-    step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     start.record()
-    for i in range(args.steps):
-        step_evs[i][0].record()
-        graphs[(args.warmup + i) % n_copies].replay()
-        step_evs[i][1].record()
+    timed_graph.replay()
     stop.record()
     barrier()
     elapsed_ms = start.elapsed_time(stop)
-    gemv_ms = sum(a.elapsed_time(b) for a, b in step_evs)
     # keep the same replays running long enough to sample clocks under load
     t_end = time.perf_counter() + 2.0
-    k = 0
     while time.perf_counter() < t_end:
-        for _ in range(200):
-            graphs[k % n_copies].replay()
-            k += 1
+        for _ in range(20):
+            timed_graph.replay()
         torch.cuda.synchronize()
     clocks = sampler.stop()
+
+    # ---------------- the GEMV kernel's own launch durations (roofline):
+    # CUDA events on the launching stream bracket every launch of the step
+    launch_evs = []
+
+    def launch_timed(i):
+        layer = copies[i % n_copies]
+        for names in launch_groups:
+            rows = [shape[n][0] for n in names]
+            cols, inp = shape[names[0]][1], shape[names[0]][2]
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            # keep the GPU busy while the host enqueues event, launch, event, so
+            # that the pair brackets the kernel alone (not the host's launch work)
+            torch.cuda._sleep(100000)
+            a.record()
+            if len(names) == 1:
+                q4k.q4k_gemv(layer[names[0]], rows[0], cols, xs[inp], y=ys[names[0]])
+            else:
+                q4k.q4k_gemv_multi([layer[n] for n in names], rows, cols, xs[inp], ys=[ys[n] for n in names])
+            b.record()
+            launch_evs.append((a, b))
+
+    for i in range(args.steps):
+        launch_timed(args.warmup + i)
+    torch.cuda.synchronize()
+    gemv_ms = sum(a.elapsed_time(b) for a, b in launch_evs)
 
     # ---------------- e2e: public API with host buffers, copies in the region
     inputs_host = {k: torch.from_numpy(v).pin_memory() for k, v in xs_np.items()}
@@ -382,38 +404,41 @@ def run_ours(args, rank, world):
     for i in range(args.warmup):
         prefill_step(i)
     torch.cuda.synchronize()
-    pgraphs, ggraphs = [], []
-    for c in range(p_copies):
+
+    def capture_fn(fn, first, count):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            prefill_step(c)
-        pgraphs.append(g)
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2):
-            gemm_only(c)
-        ggraphs.append(g2)
-    for i in range(args.warmup):
-        pgraphs[i % p_copies].replay()
+            for i in range(first, first + count):
+                fn(i)
+        return g
+
+    pwarm = capture_fn(prefill_step, 0, args.warmup)
+    ptimed = capture_fn(prefill_step, args.warmup, args.steps)
+    gwarm = capture_fn(gemm_only, 0, args.warmup)
+    gtimed = capture_fn(gemm_only, args.warmup, args.steps)
+    pwarm.replay()
     barrier()
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     p0.record()
-    for i in range(args.steps):
-        pgraphs[(args.warmup + i) % p_copies].replay()
+    ptimed.replay()
     p1.record()
     barrier()
     prefill_ms = p0.elapsed_time(p1)
     # the GEMM launches alone (same inputs), for the GEMM's own roofline
-    for i in range(args.warmup):
-        ggraphs[i % p_copies].replay()
+    gwarm.replay()
     torch.cuda.synchronize()
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     g0.record()
-    for i in range(args.steps):
-        ggraphs[(args.warmup + i) % p_copies].replay()
+    gtimed.replay()
     g1.record()
     torch.cuda.synchronize()
     gemm_ms = g0.elapsed_time(g1)
     gemm_ops = 2.0 * T * (9728 * 2560 + 2560 * 9728)
+    # tensor-core rate probes on this GPU: the int8 rate of the warp-level
+    # MMA (mma.sync m16n8k32 s8) and the fp16 rate of tcgen05.mma kind::f16
+    from q4_weight_matmul_gb300 import peaks as tc_peaks
+    int8_peak = tc_peaks.mma_s8_tops(iters=20000)
+    f16_peak = tc_peaks.tc_f16_tflops(groups=2048)
 
     # ---------------- reduce over ranks (max time), sum of work
     def max_over_ranks(v):
@@ -451,15 +476,17 @@ def run_ours(args, rank, world):
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "parallelism": "replicas" if world > 1 else "single",
-                   "timing": "each step is one CUDA-graph replay of the layer's 4 GEMV launches "
-                             "(QKV fused, o, gate/up fused, down), programmatic dependent launches",
+                   "timing": "one CUDA graph of exactly `steps` layer steps; each step is the layer's 4 GEMV "
+                             "launches (QKV fused, o, gate/up fused, down)",
                    "l2": f"inputs larger than L2: {n_copies} rotating layer copies "
                          f"({n_copies * layer_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
                    "launches_per_step": n_launch},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": f"{peak_kind} hbm_gbs",
                      "kernel": "gemv_block144_kernel<1>",
-                     "duration": "graph-replayed step time over its 4 launches (includes launch gaps)"},
+                     "duration": "CUDA events around each of the step's 4 launches (eager, each launch "
+                                 "queued behind a sleep kernel so the events bracket the kernel alone), "
+                                 "summed over the timed steps"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": n_launch * args.steps,
         "clocks": clocks,
@@ -471,10 +498,15 @@ def run_ours(args, rank, world):
             "tok_s": T * args.steps * world / (prefill_ms * 1e-3),
             "int_tops": gemm_ops * args.steps * world / (prefill_ms * 1e-3) / 1e12,
             "gemm_tops": gemm_tops,
-            "roofline": {"bound": "tensor", "achieved": gemm_tops, "unit": "TOPS",
-                         "peak_bf16_dense": bf16, "frac_of_bf16_peak": gemm_tops / bf16},
+            # the GEMM's MMAs are tcgen05 kind::f16 (exact small integers in
+            # fp16), so its own-dtype peak is the dense fp16 = bf16 rate
+            "roofline": {"bound": "tensor", "achieved": gemm_tops, "unit": "TOPS", "peak": bf16,
+                         "frac": gemm_tops / bf16, "peak_kind": f"{peak_kind} bf16_tflops (fp16 rate)",
+                         "int8_peak_mma_sync_s8": int8_peak, "frac_of_int8_peak": gemm_tops / int8_peak,
+                         "tcgen05_f16_probe_tflops": f16_peak},
             "gpu_launches": 4 * args.steps,
-            "timing": "CUDA-graph replays; gemm_tops from the GEMM launches alone",
+            "timing": "one CUDA graph of exactly `steps` steps (q8_1 + GEMM for gate and down); "
+                      "gemm_tops from a graph of the GEMM launches alone",
             "l2": f"{p_copies} rotating weight+input copies",
         },
     }

@@ -92,3 +92,10 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 256)
     with pytest.raises(TypeError):
         q4k.q8_quantize(x)
+
+
+def test_rate_probe_library_loads_and_exports_its_probes(lib):
+    from q4_weight_matmul_gb300.build import PEAKS_LIB
+    probe = ctypes.CDLL(PEAKS_LIB)
+    for name in ("q4kp_mma_s8_tops", "q4kp_tc_f16_tflops"):
+        assert hasattr(probe, name), name

@@ -330,7 +330,7 @@ def run_ours(args, rank, world):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             # keep the GPU busy while the host enqueues event, launch, event, so
             # that the pair brackets the kernel alone (not the host's launch work)
-            torch.cuda._sleep(100000)
+            torch.cuda._sleep(1000000)
             a.record()
             if len(names) == 1:
                 q4k.q4k_gemv(layer[names[0]], rows[0], cols, xs[inp], y=ys[names[0]])

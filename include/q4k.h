@@ -150,6 +150,17 @@ int q4k_gemm_blockdots(const void* w, int layout, int64_t rows, int64_t cols,
  */
 int q4k_device_error(void* stream);
 
+/*
+ * q4k_selftest_wait_timeout - test export of the failure-detection path (no
+ * counterpart on the pages): enqueues on `stream` a one-thread kernel whose
+ * only wait is on a barrier that nothing completes.  The wait is bounded
+ * like every wait in the library's kernels; after its limit (about two
+ * seconds at the maximum SM clock) the kernel records a timeout in the
+ * device error word and exits normally.  A following q4k_device_error()
+ * then returns Q4K_ERR_DEVICE_TIMEOUT, and the context remains usable.
+ */
+int q4k_selftest_wait_timeout(void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* q4k_status_string(int status);
 

@@ -35,6 +35,7 @@ SIGNATURES = {
     "q4k_gemm": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
     "q4k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
     "q4k_device_error": (_I, [_P]),
+    "q4k_selftest_wait_timeout": (_I, [_P]),
     "q4k_status_string": (ctypes.c_char_p, [_I]),
     "q4k_last_error_string": (ctypes.c_char_p, []),
     "q4k_version": (ctypes.c_char_p, []),
@@ -187,10 +188,17 @@ def q4k_device_error(stream=None) -> int:
     return int(lib().q4k_device_error(_stream(stream)))
 
 
+def q4k_selftest_wait_timeout(stream=None) -> None:
+    """Enqueue the library's bounded-wait self-test kernel (see q4k.h); the
+    next ``q4k_device_error`` reports the timeout it records."""
+    _check(lib().q4k_selftest_wait_timeout(_stream(stream)), "q4k_selftest_wait_timeout")
+
+
 def q4k_version() -> str:
     return lib().q4k_version().decode()
 
 
 __all__ = ["build", "lib", "Q4KError", "BLOCK144", "q4k_packed_bytes", "q4k_pack", "q8_quantize",
-           "q4k_gemv", "q4k_gemv_multi", "q4k_gemm", "q4k_gemm_blockdots", "q4k_device_error", "q4k_version",
+           "q4k_gemv", "q4k_gemv_multi", "q4k_gemm", "q4k_gemm_blockdots", "q4k_device_error",
+           "q4k_selftest_wait_timeout", "q4k_version",
            "SIGNATURES"]

@@ -223,6 +223,13 @@ int q4k_gemm_blockdots(const void* w, int layout, int64_t rows, int64_t cols, co
   return gemm_common(w, layout, rows, cols, q8, nullptr, nullptr, tokens, nullptr, p, stream);
 }
 
+int q4k_selftest_wait_timeout(void* stream) {
+  int* err = device_error_word();
+  if (!err) return record_cuda(cudaGetLastError());
+  cudaError_t e = launch_wait_timeout_selftest(err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
 int q4k_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return record_cuda(e);

@@ -228,11 +228,13 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
       int slot = 0, g = rb0, sj = 0;
       int m = mat_of(P, g);
       uint32_t phase = 0;
+      int issued = 0;
       for (int j = 0; j < n_stages; ++j) {
         if (!tc::mbar_wait_sleep(&empty[slot], phase ^ 1)) {
           atomicOr(P.err, 2);
           break;
         }
+        ++issued;
         tc::mbar_arrive_expect_tx(&full[slot], kStageBytes);
         tc::tma_load_3d(stages + (size_t)slot * kStageBytes, &P.map[m], 0, (g - P.rb_start[m]) * RB, sj * SB,
                         &full[slot]);
@@ -246,6 +248,10 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
           phase ^= 1;
         }
       }
+      // every copy issued has landed before this warp (and so the CTA) exits,
+      // even if consumers gave up a wait and left early (bounded as well)
+      for (int j = max(0, issued - ring); j < issued; ++j)
+        if (!tc::mbar_wait_sleep(&full[j % ring], (uint32_t)((j / ring) & 1))) atomicOr(P.err, 2);
     }
     if (P.trigger_late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     return;

@@ -58,4 +58,8 @@ cudaError_t launch_gemm_block144(const uint8_t* w, int64_t rows, int64_t cols,
                                  const int32_t* sum, int64_t tokens, float* y,
                                  int32_t* p_out, int* err, cudaStream_t s);
 
+// One-thread kernel whose only (bounded) wait can never complete: after the
+// library's wait limit it records a timeout in `err` and returns.
+cudaError_t launch_wait_timeout_selftest(int* err, cudaStream_t s);
+
 }  // namespace q4k

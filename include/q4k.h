@@ -97,6 +97,10 @@ int q8_quantize(const float* x, int64_t tokens, int64_t cols, int8_t* q,
  *   residual : float [batch][rows] or NULL
  *   y        : float [batch][rows]; may alias residual, not x or w
  * Accuracy: |y - exact| <= 1e-4 * sum_k |w||x| (+|residual|) per element.
+ * Arithmetic: each 32-wide block of x is held as a 23-bit fixed-point
+ * integer with a power-of-two scale (error <= 2^-22 of the block's largest
+ * |x| per element), the quant-times-x block sums are exact integers, and the
+ * scales d*sc, dmin*m are applied in fp32.
  * Deterministic: the same inputs give the same bits on every run.
  */
 int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols,

@@ -26,13 +26,17 @@
 // chunk.  A chunk's 32 quant bytes hold sub-block 2c in low nibbles and 2c+1
 // in high nibbles.
 //
-// Dequantisation.  A nibble at bit position p (p <= 16) ORed into the float
-// 2^23 gives 2^23 + q*2^p exactly; subtracting 2^23 leaves q*2^p, and the
-// activation staged for that position is pre-multiplied by 2^-p, so the
-// product is exactly q*x before its fp32 rounding.  A word of eight nibbles
-// costs one shift, eight LOP3s, four fp32x2 adds and four fp32x2 FMAs (per
-// token), written in PTX so that the pairs are formed in place.  Per
-// sub-block j:  acc += d*sc_j*P_j - dmin*m_j*X_j  with X_j = sum of x over j.
+// Arithmetic.  Each 32-wide sub-block j of the activations is staged as a
+// 23-bit fixed-point integer X = rint(x / s_j) with a power-of-two scale
+// s_j = 2^(e-22), e the exponent of the sub-block's largest |x| (so
+// |X| <= 2^22 and |x - s_j*X| <= s_j/2 <= 2^-22 * max|x|), split into three
+// byte planes X = 65536*X2 + 256*X1 + X0 (X0, X1 unsigned, X2 signed).  The
+// 4-bit quants q enter dp4a dot products with the planes unchanged, so
+// P_j = sum q*X over the sub-block is an exact integer; the per-sub-block
+// scales are applied in fp32 registers:
+//     acc += d*sc_j*s_j*P_j - dmin*m_j*XS_j,    XS_j = sum of x over j.
+// A 32-bit word of quants (8 weights) costs a shift, two LOP3s and six dp4a
+// per token, against one fp32 multiply-add per weight for a dequantised dot.
 #include "q4k_internal.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -50,7 +54,7 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;     // + one producer warp
-constexpr int kRegion = 68;                   // floats per (token, superblock, chunk): 32 (lo,hi) pairs + pad
+constexpr int kRegion = 208;                  // bytes per (token, superblock, chunk) of x planes: 192 + pad
 constexpr int kStageSuper = 128;              // superblock-rows per stage (RB * SB)
 constexpr int kStageBytes = kStageSuper * kBlockBytes;
 constexpr int kMaxRing = 6;
@@ -74,41 +78,17 @@ __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
 }
 
-// Eight nibbles of v -> four exact (q_lo*2^p, q_hi*2^p) fp32 pairs.
-__device__ __forceinline__ void conv_word(uint32_t v, uint64_t& f0, uint64_t& f1, uint64_t& f2,
-                                          uint64_t& f3) {
-  asm("{\n\t.reg .b32 a0,a1,a2,a3,a4,a5,a6,a7,v12;\n\t"
-      "shr.b32 v12, %4, 12;\n\t"
-      "lop3.b32 a0, %4, 0xF, 0x4B000000, 0xEA;\n\t"
-      "lop3.b32 a1, %4, 0xF0, 0x4B000000, 0xEA;\n\t"
-      "lop3.b32 a2, %4, 0xF00, 0x4B000000, 0xEA;\n\t"
-      "lop3.b32 a3, %4, 0xF000, 0x4B000000, 0xEA;\n\t"
-      "lop3.b32 a4, %4, 0xF0000, 0x4B000000, 0xEA;\n\t"
-      "lop3.b32 a5, v12, 0xF00, 0x4B000000, 0xEA;\n\t"
-      "lop3.b32 a6, v12, 0xF000, 0x4B000000, 0xEA;\n\t"
-      "lop3.b32 a7, v12, 0xF0000, 0x4B000000, 0xEA;\n\t"
-      "mov.b64 %0, {a0, a1};\n\tmov.b64 %1, {a2, a3};\n\tmov.b64 %2, {a4, a5};\n\tmov.b64 %3, {a6, a7};\n\t"
-      "add.rn.f32x2 %0, %0, %5;\n\tadd.rn.f32x2 %1, %1, %5;\n\t"
-      "add.rn.f32x2 %2, %2, %5;\n\tadd.rn.f32x2 %3, %3, %5;\n\t}"
-      : "=l"(f0), "=l"(f1), "=l"(f2), "=l"(f3)
-      : "r"(v), "l"(0xCB000000CB000000ull));
+// acc += dot of the four unsigned bytes of a and of b
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int acc) {
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(acc));
+  return d;
 }
-
-// pe += f0*x(0,1) + f2*x(4,5); po += f1*x(2,3) + f3*x(6,7)
-__device__ __forceinline__ void fma_word(uint64_t f0, uint64_t f1, uint64_t f2, uint64_t f3,
-                                         const uint4& xa, const uint4& xc, uint64_t& pe, uint64_t& po) {
-  asm("{\n\t.reg .b64 x0,x1,x2,x3;\n\t"
-      "mov.b64 x0, {%6, %7};\n\tmov.b64 x1, {%8, %9};\n\t"
-      "mov.b64 x2, {%10, %11};\n\tmov.b64 x3, {%12, %13};\n\t"
-      "fma.rn.f32x2 %0, %2, x0, %0;\n\tfma.rn.f32x2 %1, %3, x1, %1;\n\t"
-      "fma.rn.f32x2 %0, %4, x2, %0;\n\tfma.rn.f32x2 %1, %5, x3, %1;\n\t}"
-      : "+l"(pe), "+l"(po)
-      : "l"(f0), "l"(f1), "l"(f2), "l"(f3), "r"(xa.x), "r"(xa.y), "r"(xa.z), "r"(xa.w), "r"(xc.x),
-        "r"(xc.y), "r"(xc.z), "r"(xc.w));
-}
-
-__device__ __forceinline__ float2 u64_as_f2(uint64_t v) {
-  return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
+// acc += dot of the four unsigned bytes of a and the four signed bytes of b
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int acc) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(acc));
+  return d;
 }
 
 // byte i of w as a float (exact)
@@ -121,11 +101,11 @@ struct Layout {
 __host__ __device__ inline Layout layout(int B, int nb, int ring, int part_floats) {
   Layout L;
   L.xs = 0;
-  L.xsum = L.xs + sizeof(float) * (size_t)B * nb * 4 * kRegion;
-  L.part = L.xsum + sizeof(float) * (size_t)B * nb * 8;
+  L.xsum = L.xs + (size_t)B * nb * 4 * kRegion;
+  L.part = L.xsum + sizeof(float2) * (size_t)B * nb * 8;
   L.stages = (L.part + sizeof(float) * (size_t)part_floats + 1023) & ~size_t(1023);
   L.bars = L.stages + (size_t)ring * kStageBytes;
-  L.total = L.bars + sizeof(uint64_t) * 2 * ring + 1024;   // + slack to align the base
+  L.total = L.bars + sizeof(uint64_t) * 2 * ring + 16 + 1024;   // + issue counter, + slack to align the base
   return L;
 }
 
@@ -138,11 +118,15 @@ __device__ __forceinline__ int mat_of(const GemvParams& P, int g) {
   return m;
 }
 
-// Activations staged once: pre-scaled by 2^-p, (lo, hi)-paired per chunk, and
-// summed over each 32-wide sub-block.  All loads of a round are issued before
-// any use; eight lanes hold one sub-block, so its sum is three shuffles.
+// Activations staged once per CTA as byte planes of 23-bit fixed point (see
+// the file comment), with each sub-block's scale s_j and fp32 sum XS_j.
+// Eight lanes hold one sub-block (four elements each), so its max and sum
+// are three shuffles; all loads of a round are issued before any use.
+// Plane layout per (token, superblock, chunk c): 16-byte words at
+// ((h*3 + p)*2 + s)*16, h = half of the chunk's 32 positions, p = plane,
+// s = sub-block 2c (0) or 2c+1 (1); word k of it holds positions 16h+4k..+3.
 template <int B>
-__device__ __forceinline__ void stage_x(const float* __restrict__ x, int nb, float* xs, float* xsum,
+__device__ __forceinline__ void stage_x(const float* __restrict__ x, int nb, uint8_t* xs, float2* xss,
                                         int tid) {
   const int row4 = nb * 64;                     // float4 per activation row
   const int n4 = B * row4;                      // a multiple of 64: whole warps
@@ -159,29 +143,51 @@ __device__ __forceinline__ void stage_x(const float* __restrict__ x, int nb, flo
       const int idx = base + u * kConsumers;
       if (idx < n4) {
         const int b = idx / row4, k = 4 * (idx - b * row4);
-        const int s = k >> 8, r = k & 255, c = r >> 6, t = r & 63;
-        const int hi = t >> 5, l = t & 31;
-        float* dst = xs + (((size_t)b * nb + s) * 4 + c) * kRegion + 2 * l + hi;
-        // scale exponents of l%4 = 0..3: low half 0, 8, 16, 12; high half 4, 12, 8, 16
-        if (hi) {
-          dst[0] = v[u].x * 0x1p-4f;
-          dst[2] = v[u].y * 0x1p-12f;
-          dst[4] = v[u].z * 0x1p-8f;
-          dst[6] = v[u].w * 0x1p-16f;
-        } else {
-          dst[0] = v[u].x;
-          dst[2] = v[u].y * 0x1p-8f;
-          dst[4] = v[u].z * 0x1p-16f;
-          dst[6] = v[u].w * 0x1p-12f;
-        }
+        const int sb = k >> 8, r = k & 255, j = r >> 5, pos = r & 31;
+        const int c = j >> 1, sf = j & 1, h = pos >> 4, kw = (pos & 15) >> 2;
+        float amax = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
         float sum = (v[u].x + v[u].y) + (v[u].z + v[u].w);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        if ((idx & 7) == 0) xsum[(size_t)b * nb * 8 + (k >> 5)] = sum;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        }
+        // power-of-two scale: |x| < 2^(E-126) for the biased exponent E of
+        // amax, so X = rint(x * 2^(148-E)) satisfies |X| <= 2^22; blocks
+        // below 2^-104 (and all-zero blocks) are staged as zero
+        const int E = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+        const bool live = E >= 22;
+        const float mul = live ? __uint_as_float((uint32_t)(275 - E) << 23) : 0.0f;
+        const float scale = live ? __uint_as_float((uint32_t)(E - 21) << 23) : 0.0f;
+        const int X0 = __float2int_rn(v[u].x * mul), X1 = __float2int_rn(v[u].y * mul);
+        const int X2 = __float2int_rn(v[u].z * mul), X3 = __float2int_rn(v[u].w * mul);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(xs + (((size_t)b * nb + sb) * 4 + c) * kRegion) +
+                        (h * 3 * 2 + sf) * 4 + kw;
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl) {
+          const int sh = 8 * pl;
+          const uint32_t word = ((uint32_t)(X0 >> sh) & 0xFFu) | (((uint32_t)(X1 >> sh) & 0xFFu) << 8) |
+                                (((uint32_t)(X2 >> sh) & 0xFFu) << 16) | (((uint32_t)(X3 >> sh) & 0xFFu) << 24);
+          dst[pl * 2 * 4] = word;
+        }
+        if ((idx & 7) == 0) xss[((size_t)b * nb + sb) * 8 + j] = make_float2(scale, sum);
       }
     }
   }
+}
+
+// Bounded spin until the producer has issued stage j (false on timeout).
+__device__ __noinline__ bool wait_issued(volatile int* issued, int j) {
+  const long long t0 = clock64();
+  while (*issued <= j) {
+    __nanosleep(64);
+    if (clock64() - t0 > tc::kTimeoutCycles) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
+  return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }
 
 // LPR: lanes per row (1, 2 or 4); RB = 32 / LPR rows per block.
@@ -202,12 +208,13 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
   const int n_sj = (nb + SB - 1) / SB;      // stages per row block
   const int n_stages = my_rb * n_sj;
   const Layout L = layout(B, nb, ring, B * rb_pass * nb * RB);
-  float* xs = reinterpret_cast<float*>(smem + L.xs);
-  float* xsum = reinterpret_cast<float*>(smem + L.xsum);
+  uint8_t* xs = smem + L.xs;
+  float2* xss = reinterpret_cast<float2*>(smem + L.xsum);
   float* part = reinterpret_cast<float*>(smem + L.part);      // [B][rb of the pass][nb][RB]
   uint8_t* stages = smem + L.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ring;
+  volatile int* issued = reinterpret_cast<volatile int*>(empty + ring);   // stages issued so far
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
@@ -218,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
       tc::mbar_init(&full[i], 1);
       tc::mbar_init(&empty[i], SB);
     }
+    *issued = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -228,16 +236,18 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
       int slot = 0, g = rb0, sj = 0;
       int m = mat_of(P, g);
       uint32_t phase = 0;
-      int issued = 0;
+      int n_issued = 0;
       for (int j = 0; j < n_stages; ++j) {
         if (!tc::mbar_wait_sleep(&empty[slot], phase ^ 1)) {
           atomicOr(P.err, 2);
           break;
         }
-        ++issued;
+        ++n_issued;
         tc::mbar_arrive_expect_tx(&full[slot], kStageBytes);
         tc::tma_load_3d(stages + (size_t)slot * kStageBytes, &P.map[m], 0, (g - P.rb_start[m]) * RB, sj * SB,
                         &full[slot]);
+        __threadfence_block();
+        *issued = j + 1;
         if (++sj == n_sj) {
           sj = 0;
           ++g;
@@ -250,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
       }
       // every copy issued has landed before this warp (and so the CTA) exits,
       // even if consumers gave up a wait and left early (bounded as well)
-      for (int j = max(0, issued - ring); j < issued; ++j)
+      for (int j = max(0, n_issued - ring); j < n_issued; ++j)
         if (!tc::mbar_wait_sleep(&full[j % ring], (uint32_t)((j / ring) & 1))) atomicOr(P.err, 2);
     }
     if (P.trigger_late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -259,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
 
   // -------------------------------------------------------------- consumers
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<B>(P.x, nb, xs, xsum, tid);
+  stage_x<B>(P.x, nb, xs, xss, tid);
   named_sync_consumers();
 
   const int r_in = lane / LPR;              // row inside the block
@@ -280,6 +290,15 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
       const uint32_t phase = (uint32_t)((j / ring) & 1);
       const int rbl = jl / n_sj, sj = jl - rbl * n_sj;
       const int sb = sj * SB + z;
+      // A warp only takes its own units, so it may reach stage j while the
+      // copy of stage j - ring (same slot, same parity two phases back) is
+      // still in flight; the parity wait is unambiguous only once the
+      // producer has issued stage j, which it does after stage j - ring
+      // has landed and been consumed.
+      if (ok && *issued <= j && !wait_issued(issued, j)) {
+        ok = false;
+        if (lane == 0) atomicOr(P.err, 2);
+      }
       if (ok && !tc::mbar_wait_sleep(&full[slot], phase)) {
         ok = false;
         if (lane == 0) atomicOr(P.err, 2);
@@ -304,23 +323,40 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
           const int c = c0 + cc;
           const uint4 q0 = *reinterpret_cast<const uint4*>(p + 16 + 32 * c);
           const uint4 q1 = *reinterpret_cast<const uint4*>(p + 32 + 32 * c);
-          uint64_t pe[B], po[B];
+          // exact integer sums of q * X per plane, low (sub-block 2c) and
+          // high (2c+1) nibbles
+          int lo[B][3], hi[B][3];
 #pragma unroll
-          for (int b = 0; b < B; ++b) pe[b] = po[b] = 0ull;
-          const float* xc0 = xs + ((size_t)sb * 4 + c) * kRegion;
+          for (int b = 0; b < B; ++b)
+#pragma unroll
+            for (int pl = 0; pl < 3; ++pl) lo[b][pl] = hi[b][pl] = 0;
+          const uint8_t* xc0 = xs + ((size_t)sb * 4 + c) * kRegion;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint4 qq = h ? q1 : q0;
-            const uint32_t words[4] = {qq.x, qq.y, qq.z, qq.w};
+            uint32_t ql[4], qh[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              uint64_t f0, f1, f2, f3;
-              conv_word(words[k], f0, f1, f2, f3);
+              const uint32_t w = word_of(qq, k);
+              ql[k] = w & 0x0F0F0F0Fu;
+              qh[k] = (w >> 4) & 0x0F0F0F0Fu;
+            }
 #pragma unroll
-              for (int b = 0; b < B; ++b) {
-                const uint4* xp =
-                    reinterpret_cast<const uint4*>(xc0 + (size_t)b * nb * 4 * kRegion + 2 * (16 * h + 4 * k));
-                fma_word(f0, f1, f2, f3, xp[0], xp[1], pe[b], po[b]);
+            for (int b = 0; b < B; ++b) {
+              const uint4* xp = reinterpret_cast<const uint4*>(xc0 + (size_t)b * nb * 4 * kRegion) + h * 6;
+#pragma unroll
+              for (int pl = 0; pl < 3; ++pl) {
+                const uint4 xl = xp[2 * pl], xh = xp[2 * pl + 1];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  if (pl < 2) {
+                    lo[b][pl] = dp4a_uu(ql[k], word_of(xl, k), lo[b][pl]);
+                    hi[b][pl] = dp4a_uu(qh[k], word_of(xh, k), hi[b][pl]);
+                  } else {
+                    lo[b][pl] = dp4a_us(ql[k], word_of(xl, k), lo[b][pl]);
+                    hi[b][pl] = dp4a_us(qh[k], word_of(xh, k), hi[b][pl]);
+                  }
+                }
               }
             }
           }
@@ -331,10 +367,12 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
           const float m_lo = byte_f(mw, bi), m_hi = byte_f(mw, bi + 1);
 #pragma unroll
           for (int b = 0; b < B; ++b) {
-            const float2 a = u64_as_f2(pe[b]), o = u64_as_f2(po[b]);
-            const float2 xsm = *reinterpret_cast<const float2*>(xsum + (size_t)b * nb * 8 + sb * 8 + 2 * c);
-            scaled[b] = fmaf(sc_hi, a.y + o.y, fmaf(sc_lo, a.x + o.x, scaled[b]));
-            mins[b] = fmaf(m_hi, xsm.y, fmaf(m_lo, xsm.x, mins[b]));
+            // P = 65536*P2 + (256*P1 + P0); the bracket is an exact int32
+            const float p_lo = fmaf((float)lo[b][2], 65536.0f, (float)(lo[b][1] * 256 + lo[b][0]));
+            const float p_hi = fmaf((float)hi[b][2], 65536.0f, (float)(hi[b][1] * 256 + hi[b][0]));
+            const float4 ss = *reinterpret_cast<const float4*>(xss + ((size_t)b * nb + sb) * 8 + 2 * c);
+            scaled[b] = fmaf(sc_hi * ss.z, p_hi, fmaf(sc_lo * ss.x, p_lo, scaled[b]));
+            mins[b] = fmaf(m_hi, ss.w, fmaf(m_lo, ss.y, mins[b]));
           }
         }
 #pragma unroll

@@ -69,6 +69,7 @@ struct GemvParams {
   int rb_start[kMaxMats + 1];   // prefix sums of row blocks per matrix
   int n_mats;
   int nb, rb_per_cta, rb_pass, ring;
+  int pdl;                      // launched as a programmatic dependent
   int trigger_late;             // launch dependents after the units, not at start
   const float* x;
   int* err;
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
   const int warp = tid >> 5, lane = tid & 31;
 
   // the next kernel in the stream may start its own weight stream now
-  if (!P.trigger_late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (P.pdl && !P.trigger_late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < ring; ++i) {
       tc::mbar_init(&full[i], 1);
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
   }
 
   // -------------------------------------------------------------- consumers
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (P.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
   stage_x<B>(P.x, nb, xs, xss, tid);
   named_sync_consumers();
 
@@ -527,6 +528,7 @@ cudaError_t launch_b(const uint8_t* const* w, const int64_t* rows, int n_mats, i
   params.rb_per_cta = p.rb_per_cta;
   params.rb_pass = p.rb_pass;
   params.ring = p.ring;
+  params.pdl = pdl_mode() != 0 ? 1 : 0;
   params.trigger_late = pdl_mode() == 2 ? 1 : 0;
   params.x = x;
   switch (p.lpr) {

@@ -79,6 +79,25 @@ def profile_traffic(kernel_tag: str, source: str):
     return float(m_bytes.group(1))
 
 
+# --------------------------------------------------------------------- ranks
+def reduce_max(value: float, device=None) -> float:
+    """Largest ``value`` over the ranks of the default process group (the
+    value itself when no group is initialised or it has one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job GB/s: every rank streams ``bytes_per_step`` per step (weak
+    scaling, independent replicas) and the job takes the slowest rank's time."""
+    return bytes_per_step * steps * world / (max_ms * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
@@ -442,11 +461,7 @@ def run_ours(args, rank, world):
 
     # ---------------- reduce over ranks (max time), sum of work
     def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, dev if dist is not None else None)
 
     elapsed_ms = max_over_ranks(elapsed_ms)
     e2e_ms = max_over_ranks(e2e_ms)
@@ -457,8 +472,8 @@ def run_ours(args, rank, world):
             dist.destroy_process_group()
         return 0
 
-    value = step_bytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9
-    e2e_value = step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9
+    value = job_throughput(step_bytes, args.steps, world, elapsed_ms)
+    e2e_value = job_throughput(step_bytes, args.steps, world, e2e_ms)
     achieved = step_bytes * args.steps / (gemv_ms * 1e-3) / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     traffic = profile_traffic("gemv_block144", "gemv.cu")

@@ -132,15 +132,15 @@ __device__ __forceinline__ void stage_x(const float* __restrict__ x, int nb, uin
   const int row4 = nb * 64;                     // float4 per activation row
   const int n4 = B * row4;                      // a multiple of 64: whole warps
   const float4* x4 = reinterpret_cast<const float4*>(x);
-  for (int base = tid; base < n4; base += 4 * kConsumers) {
-    float4 v[4];
+  for (int base = tid; base < n4; base += 5 * kConsumers) {
+    float4 v[5];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 5; ++u) {
       const int idx = base + u * kConsumers;
       if (idx < n4) v[u] = __ldg(x4 + idx);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 5; ++u) {
       const int idx = base + u * kConsumers;
       if (idx < n4) {
         const int b = idx / row4, k = 4 * (idx - b * row4);

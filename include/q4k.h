@@ -121,6 +121,64 @@ int q4k_gemv_multi(int n, const void* const* w, int layout, const int64_t* rows,
                    const float* const* residual, float* const* y, void* stream);
 
 /*
+ * q4k_gemv_job - one decode GEMV of a q4k_gemv_seq list:
+ *   y[b][o] = sum_k w[o][k] * x[b][k]  (+ residual[b][o] if residual != NULL)
+ */
+typedef struct q4k_gemv_job {
+  const void* w;           /* packed weights (layout), rows x cols              */
+  int64_t rows;            /* outputs; a job with 0 rows is skipped             */
+  int64_t cols;            /* inputs, a positive multiple of 256                */
+  const float* x;          /* float [batch][cols]                               */
+  const float* residual;   /* float [batch][rows] or NULL                       */
+  float* y;                /* float [batch][rows]; may alias residual           */
+  int32_t wait;            /* non-zero: x and residual are read only after every
+                              earlier job of the list has stored its y          */
+  int32_t reserved;        /* ignored; set to 0                                 */
+} q4k_gemv_job;
+
+#define Q4K_GEMV_SEQ_MAX_JOBS 256
+
+/*
+ * q4k_gemv_seq_workspace_bytes - device workspace that q4k_gemv_seq needs for
+ * this job list and batch on the current device (it depends on where the
+ * list's `wait` flags fall, on the batch and on the SM count); 0 when the
+ * request is invalid or unsupported.
+ */
+size_t q4k_gemv_seq_workspace_bytes(const q4k_gemv_job* jobs, int n_jobs, int64_t batch);
+
+/*
+ * q4k_gemv_seq - an ordered list of decode GEMVs in ONE persistent launch
+ * (genie-ai-runtime §4, Path C: the GEMVs are the hot decode kernels, and
+ * every decode step streams the whole model's weights; §2: decode is bound
+ * by memory bandwidth).  One CTA per SM streams the weights of job after job
+ * without a launch boundary; a job with `wait` set reads its activations
+ * only after every earlier job has completed, so it may consume an earlier
+ * job's y (a decode layer: QKV | o | gate,up | down, each waiting on the
+ * previous).  Jobs between two `wait` points may run concurrently: none of
+ * them may read what another of them writes.
+ *   jobs      : HOST array of n_jobs (0..Q4K_GEMV_SEQ_MAX_JOBS) entries, read
+ *               during the call only; device pointers as in q4k_gemv
+ *   batch     : 1..8 activation rows per job (0: nothing to do)
+ *   workspace : device memory of at least q4k_gemv_seq_workspace_bytes()
+ *               bytes, 16-byte aligned, zero-filled before its first use
+ *               (e.g. cudaMemset).  It holds the launch's arrival
+ *               counters, which each call resets before it ends (also when
+ *               its kernel gave up a bounded wait), so the workspace is
+ *               reused without clearing.  Calls that share a workspace must
+ *               not overlap on the GPU.
+ * The launch is cooperative (every CTA resident at once, one per SM); it
+ * fails with Q4K_ERR_CUDA when the GPU cannot hold them all.
+ * Accuracy as q4k_gemv: |y - exact| <= 1e-4 * sum_k |w||x| (+|residual|).
+ * Deterministic: for one job list on one device, the same inputs give the
+ * same bits on every run.
+ * Errors: Q4K_ERR_INVALID_ARG (null pointer, bad size, workspace too small),
+ * Q4K_ERR_ALIGNMENT, Q4K_ERR_UNSUPPORTED (more jobs than the maximum, batch
+ * above 8, activations too wide to stage in shared memory).
+ */
+int q4k_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * q4k_gemm - prefill MMQ GEMM (genie-ai-runtime §3, "The tensor-core kernel
  * (Path E)"; integer form over q8_1 activations):
  *   y[t][o] = sum_b ( d*sc[o,b] * d8[t,b] * P[t,o,b]

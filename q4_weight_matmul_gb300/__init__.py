@@ -24,14 +24,25 @@ QK_SUB = 32
 _STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_INVALID_ARG", 2: "Q4K_ERR_ALIGNMENT",
            3: "Q4K_ERR_UNSUPPORTED", 4: "Q4K_ERR_CUDA", 5: "Q4K_ERR_DEVICE_TIMEOUT"}
 
-# Every symbol the header declares, with its ctypes signature.
 _P, _I64, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+GEMV_SEQ_MAX_JOBS = 256
+
+
+class GemvJob(ctypes.Structure):
+    """``q4k_gemv_job`` of the C ABI (one GEMV of a ``q4k_gemv_seq`` list)."""
+    _fields_ = [("w", _P), ("rows", _I64), ("cols", _I64), ("x", _P), ("residual", _P), ("y", _P),
+                ("wait", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+# Every symbol the header declares, with its ctypes signature.
 SIGNATURES = {
     "q4k_packed_bytes": (ctypes.c_size_t, [_I64, _I64, _I]),
     "q4k_pack": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _P, _P]),
     "q8_quantize": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q4k_gemv": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P, _P]),
     "q4k_gemv_multi": (_I, [_I, _P, _I, _P, _I64, _P, _I64, _P, _P, _P]),
+    "q4k_gemv_seq_workspace_bytes": (ctypes.c_size_t, [_P, _I, _I64]),
+    "q4k_gemv_seq": (_I, [_P, _I, _I, _I64, _P, ctypes.c_size_t, _P]),
     "q4k_gemm": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
     "q4k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
     "q4k_device_error": (_I, [_P]),
@@ -159,6 +170,51 @@ def q4k_gemv_multi(ws, rows, cols: int, x, residuals=None, ys=None, layout: int 
     return ys
 
 
+class GemvSeq:
+    """A prepared ``q4k_gemv_seq`` job list: the C job array and a zeroed
+    workspace, built once; calling it enqueues the one persistent launch.
+
+    ``jobs`` is a sequence of dicts with keys ``w`` (packed uint8), ``rows``,
+    ``cols``, ``x`` ([batch][cols] float32), ``y`` ([batch][rows] float32),
+    optional ``residual`` and ``wait`` (read x only after every earlier job
+    has stored its y).  The tensors must stay alive while the list is used.
+    """
+
+    def __init__(self, jobs, batch: int, layout: int = BLOCK144, workspace=None):
+        n = len(jobs)
+        arr = (GemvJob * max(n, 1))()
+        dev = None
+        for i, j in enumerate(jobs):
+            arr[i].w = _ptr(j["w"], torch.uint8, "w")
+            arr[i].rows = int(j["rows"])
+            arr[i].cols = int(j["cols"])
+            arr[i].x = _ptr(j["x"], torch.float32, "x")
+            arr[i].residual = _ptr(j.get("residual"), torch.float32, "residual")
+            arr[i].y = _ptr(j["y"], torch.float32, "y")
+            arr[i].wait = 1 if j.get("wait") else 0
+            dev = j["x"].device if dev is None else dev
+        self.jobs, self.n, self.batch, self.layout = arr, n, int(batch), layout
+        need = int(lib().q4k_gemv_seq_workspace_bytes(arr, n, self.batch)) if n else 0
+        if workspace is None:
+            workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+        elif workspace.numel() < need:
+            raise ValueError(f"workspace holds {workspace.numel()} bytes, the job list needs {need}")
+        self.workspace = workspace
+        self.workspace_bytes = need
+
+    def __call__(self, stream=None):
+        _check(lib().q4k_gemv_seq(self.jobs, self.n, self.layout, self.batch,
+                                  _ptr(self.workspace, torch.uint8, "workspace"),
+                                  self.workspace.numel(), _stream(stream)), "q4k_gemv_seq")
+
+
+def q4k_gemv_seq(jobs, batch: int, layout: int = BLOCK144, workspace=None, stream=None):
+    """One persistent launch over an ordered GEMV job list (see ``GemvSeq``)."""
+    seq = GemvSeq(jobs, batch, layout, workspace)
+    seq(stream)
+    return seq
+
+
 def q4k_gemm(w, rows: int, cols: int, q8, d8, s, y=None, layout: int = BLOCK144, stream=None):
     """Prefill MMQ GEMM on q8_1 activations; returns ``y`` [tokens][rows] float32."""
     tokens = q8.shape[0]
@@ -199,6 +255,7 @@ def q4k_version() -> str:
 
 
 __all__ = ["build", "lib", "Q4KError", "BLOCK144", "q4k_packed_bytes", "q4k_pack", "q8_quantize",
-           "q4k_gemv", "q4k_gemv_multi", "q4k_gemm", "q4k_gemm_blockdots", "q4k_device_error",
+           "q4k_gemv", "q4k_gemv_multi", "GemvJob", "GemvSeq", "q4k_gemv_seq", "q4k_gemm",
+           "q4k_gemm_blockdots", "q4k_device_error",
            "q4k_selftest_wait_timeout", "q4k_version",
            "SIGNATURES"]

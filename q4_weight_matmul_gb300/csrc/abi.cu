@@ -186,6 +186,29 @@ int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols, const float*
   return q4k_gemv_multi(1, &w, layout, &rows, cols, x, batch, res, ys, stream);
 }
 
+// Host-side checks of a q4k_gemv_seq request (no CUDA call).  Sets *work to
+// whether any job has work.
+static int check_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch, bool* work) {
+  *work = false;
+  if (n_jobs < 0) return Q4K_ERR_INVALID_ARG;
+  if (n_jobs > kGemvSeqMaxJobs) return Q4K_ERR_UNSUPPORTED;
+  if (n_jobs > 0 && !jobs) return Q4K_ERR_INVALID_ARG;
+  if (int e = check_layout(layout)) return e;
+  if (batch < 0 || batch > 8) return batch < 0 ? Q4K_ERR_INVALID_ARG : Q4K_ERR_UNSUPPORTED;
+  for (int i = 0; i < n_jobs; ++i) {
+    const q4k_gemv_job& j = jobs[i];
+    if (int e = check_rows(j.rows)) return e;
+    if (int e = check_cols(j.cols)) return e;
+    if (j.rows == 0) continue;
+    if (!j.w || !j.x || !j.y) return Q4K_ERR_INVALID_ARG;
+    if (!aligned16(j.w) || !aligned16(j.x) || !aligned16(j.y) || (j.residual && !aligned16(j.residual)))
+      return Q4K_ERR_ALIGNMENT;
+    *work = true;
+  }
+  if (batch == 0) *work = false;
+  return Q4K_OK;
+}
+
 static int gemm_common(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8,
                        const float* d8, const int32_t* sum, int64_t tokens, float* y,
                        int32_t* p, void* stream) {
@@ -221,6 +244,28 @@ int q4k_gemm_blockdots(const void* w, int layout, int64_t rows, int64_t cols, co
                        int64_t tokens, int32_t* p, void* stream) {
   if (!p && rows != 0 && tokens != 0) return Q4K_ERR_INVALID_ARG;
   return gemm_common(w, layout, rows, cols, q8, nullptr, nullptr, tokens, nullptr, p, stream);
+}
+
+size_t q4k_gemv_seq_workspace_bytes(const q4k_gemv_job* jobs, int n_jobs, int64_t batch) {
+  bool work = false;
+  if (check_seq(jobs, n_jobs, Q4K_LAYOUT_BLOCK144, batch, &work) != Q4K_OK || !work) return 0;
+  size_t bytes = 0;
+  if (gemv_seq_workspace(jobs, n_jobs, (int)batch, &bytes) != Q4K_OK) return 0;
+  return bytes;
+}
+
+int q4k_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  bool work = false;
+  if (int e = check_seq(jobs, n_jobs, layout, batch, &work)) return e;
+  if (!work) return Q4K_OK;
+  if (!workspace) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return Q4K_ERR_ALIGNMENT;
+  cudaError_t ce = cudaSuccess;
+  const int st = launch_gemv_seq(jobs, n_jobs, (int)batch, workspace, workspace_bytes,
+                                 static_cast<cudaStream_t>(stream), &ce);
+  if (st == Q4K_ERR_CUDA) return record_cuda(ce);
+  return st;
 }
 
 int q4k_selftest_wait_timeout(void* stream) {

@@ -26,17 +26,9 @@
 // chunk.  A chunk's 32 quant bytes hold sub-block 2c in low nibbles and 2c+1
 // in high nibbles.
 //
-// Arithmetic.  Each 32-wide sub-block j of the activations is staged as a
-// 23-bit fixed-point integer X = rint(x / s_j) with a power-of-two scale
-// s_j = 2^(e-22), e the exponent of the sub-block's largest |x| (so
-// |X| <= 2^22 and |x - s_j*X| <= s_j/2 <= 2^-22 * max|x|), split into three
-// byte planes X = 65536*X2 + 256*X1 + X0 (X0, X1 unsigned, X2 signed).  The
-// 4-bit quants q enter dp4a dot products with the planes unchanged, so
-// P_j = sum q*X over the sub-block is an exact integer; the per-sub-block
-// scales are applied in fp32 registers:
-//     acc += d*sc_j*s_j*P_j - dmin*m_j*XS_j,    XS_j = sum of x over j.
-// A 32-bit word of quants (8 weights) costs a shift, two LOP3s and six dp4a
-// per token, against one fp32 multiply-add per weight for a dequantised dot.
+// Arithmetic: 23-bit fixed-point activation planes and exact integer dp4a
+// block sums, scales applied in fp32 (gemv_common.cuh).
+#include "gemv_common.cuh"
 #include "q4k_internal.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -54,7 +46,6 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;     // + one producer warp
-constexpr int kRegion = 208;                  // bytes per (token, superblock, chunk) of x planes: 192 + pad
 constexpr int kStageSuper = 128;              // superblock-rows per stage (RB * SB)
 constexpr int kStageBytes = kStageSuper * kBlockBytes;
 constexpr int kMaxRing = 6;
@@ -79,22 +70,6 @@ __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
 }
 
-// acc += dot of the four unsigned bytes of a and of b
-__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int acc) {
-  int d;
-  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(acc));
-  return d;
-}
-// acc += dot of the four unsigned bytes of a and the four signed bytes of b
-__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int acc) {
-  int d;
-  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(acc));
-  return d;
-}
-
-// byte i of w as a float (exact)
-__device__ __forceinline__ float byte_f(uint32_t w, int i) { return (float)((w >> (8 * i)) & 0xFFu); }
-
 struct Layout {
   size_t xs, xsum, part, stages, bars, total;
 };
@@ -102,8 +77,8 @@ struct Layout {
 __host__ __device__ inline Layout layout(int B, int nb, int ring, int part_floats) {
   Layout L;
   L.xs = 0;
-  L.xsum = L.xs + (size_t)B * nb * 4 * kRegion;
-  L.part = L.xsum + sizeof(float2) * (size_t)B * nb * 8;
+  L.xsum = L.xs + gemv::xs_bytes(B, nb);
+  L.part = L.xsum + gemv::xss_bytes(B, nb);
   L.stages = (L.part + sizeof(float) * (size_t)part_floats + 1023) & ~size_t(1023);
   L.bars = L.stages + (size_t)ring * kStageBytes;
   L.total = L.bars + sizeof(uint64_t) * 2 * ring + 16 + 1024;   // + issue counter, + slack to align the base
@@ -117,78 +92,6 @@ __device__ __forceinline__ int mat_of(const GemvParams& P, int g) {
   for (int i = 1; i < kMaxMats; ++i)
     if (i < P.n_mats && g >= P.rb_start[i]) m = i;
   return m;
-}
-
-// Activations staged once per CTA as byte planes of 23-bit fixed point (see
-// the file comment), with each sub-block's scale s_j and fp32 sum XS_j.
-// Eight lanes hold one sub-block (four elements each), so its max and sum
-// are three shuffles; all loads of a round are issued before any use.
-// Plane layout per (token, superblock, chunk c): 16-byte words at
-// ((h*3 + p)*2 + s)*16, h = half of the chunk's 32 positions, p = plane,
-// s = sub-block 2c (0) or 2c+1 (1); word k of it holds positions 16h+4k..+3.
-template <int B>
-__device__ __forceinline__ void stage_x(const float* __restrict__ x, int nb, uint8_t* xs, float2* xss,
-                                        int tid) {
-  const int row4 = nb * 64;                     // float4 per activation row
-  const int n4 = B * row4;                      // a multiple of 64: whole warps
-  const float4* x4 = reinterpret_cast<const float4*>(x);
-  for (int base = tid; base < n4; base += 5 * kConsumers) {
-    float4 v[5];
-#pragma unroll
-    for (int u = 0; u < 5; ++u) {
-      const int idx = base + u * kConsumers;
-      if (idx < n4) v[u] = __ldg(x4 + idx);
-    }
-#pragma unroll
-    for (int u = 0; u < 5; ++u) {
-      const int idx = base + u * kConsumers;
-      if (idx < n4) {
-        const int b = idx / row4, k = 4 * (idx - b * row4);
-        const int sb = k >> 8, r = k & 255, j = r >> 5, pos = r & 31;
-        const int c = j >> 1, sf = j & 1, h = pos >> 4, kw = (pos & 15) >> 2;
-        float amax = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
-        float sum = (v[u].x + v[u].y) + (v[u].z + v[u].w);
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        }
-        // power-of-two scale: |x| < 2^(E-126) for the biased exponent E of
-        // amax, so X = rint(x * 2^(148-E)) satisfies |X| <= 2^22; blocks
-        // below 2^-104 (and all-zero blocks) are staged as zero
-        const int E = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
-        const bool live = E >= 22;
-        const float mul = live ? __uint_as_float((uint32_t)(275 - E) << 23) : 0.0f;
-        const float scale = live ? __uint_as_float((uint32_t)(E - 21) << 23) : 0.0f;
-        const int X0 = __float2int_rn(v[u].x * mul), X1 = __float2int_rn(v[u].y * mul);
-        const int X2 = __float2int_rn(v[u].z * mul), X3 = __float2int_rn(v[u].w * mul);
-        uint32_t* dst = reinterpret_cast<uint32_t*>(xs + (((size_t)b * nb + sb) * 4 + c) * kRegion) +
-                        (h * 3 * 2 + sf) * 4 + kw;
-#pragma unroll
-        for (int pl = 0; pl < 3; ++pl) {
-          const int sh = 8 * pl;
-          const uint32_t word = ((uint32_t)(X0 >> sh) & 0xFFu) | (((uint32_t)(X1 >> sh) & 0xFFu) << 8) |
-                                (((uint32_t)(X2 >> sh) & 0xFFu) << 16) | (((uint32_t)(X3 >> sh) & 0xFFu) << 24);
-          dst[pl * 2 * 4] = word;
-        }
-        if ((idx & 7) == 0) xss[((size_t)b * nb + sb) * 8 + j] = make_float2(scale, sum);
-      }
-    }
-  }
-}
-
-// Bounded spin until the producer has issued stage j (false on timeout).
-__device__ __noinline__ bool wait_issued(volatile int* issued, int j) {
-  const long long t0 = clock64();
-  while (*issued <= j) {
-    __nanosleep(64);
-    if (clock64() - t0 > tc::kTimeoutCycles) return false;
-  }
-  return true;
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
-  return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }
 
 // LPR: lanes per row (1, 2 or 4); RB = 32 / LPR rows per block.
@@ -270,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
 
   // -------------------------------------------------------------- consumers
   if (P.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<B>(P.x, nb, xs, xss, tid);
+  gemv::stage_x<B, kConsumers, false>(P.x, nb, xs, xss, tid);
   named_sync_consumers();
 
   const int r_in = lane / LPR;              // row inside the block
@@ -296,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
       // still in flight; the parity wait is unambiguous only once the
       // producer has issued stage j, which it does after stage j - ring
       // has landed and been consumed.
-      if (ok && *issued <= j && !wait_issued(issued, j)) {
+      if (ok && *issued <= j && !gemv::wait_issued(issued, j)) {
         ok = false;
         if (lane == 0) atomicOr(P.err, 2);
       }
@@ -310,74 +213,7 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kern
       if (sb < nb) {
         // stage laid out [SB][RB][144] (rows inner)
         const uint8_t* p = stages + (size_t)slot * kStageBytes + ((size_t)z * RB + r_in) * kBlockBytes;
-        const uint4 hd = *reinterpret_cast<const uint4*>(p);
-        const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
-        // scales (sc) and mins (m) of sub-blocks 0..3 and 4..7, one byte each
-        const uint32_t sc03 = hd.y & 0x3F3F3F3Fu, m03 = hd.z & 0x3F3F3F3Fu;
-        const uint32_t sc47 = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-        const uint32_t m47 = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-        float scaled[B], mins[B];
-#pragma unroll
-        for (int b = 0; b < B; ++b) scaled[b] = mins[b] = 0.0f;
-#pragma unroll
-        for (int cc = 0; cc < CPL; ++cc) {
-          const int c = c0 + cc;
-          const uint4 q0 = *reinterpret_cast<const uint4*>(p + 16 + 32 * c);
-          const uint4 q1 = *reinterpret_cast<const uint4*>(p + 32 + 32 * c);
-          // exact integer sums of q * X per plane, low (sub-block 2c) and
-          // high (2c+1) nibbles
-          int lo[B][3], hi[B][3];
-#pragma unroll
-          for (int b = 0; b < B; ++b)
-#pragma unroll
-            for (int pl = 0; pl < 3; ++pl) lo[b][pl] = hi[b][pl] = 0;
-          const uint8_t* xc0 = xs + ((size_t)sb * 4 + c) * kRegion;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint4 qq = h ? q1 : q0;
-            uint32_t ql[4], qh[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t w = word_of(qq, k);
-              ql[k] = w & 0x0F0F0F0Fu;
-              qh[k] = (w >> 4) & 0x0F0F0F0Fu;
-            }
-#pragma unroll
-            for (int b = 0; b < B; ++b) {
-              const uint4* xp = reinterpret_cast<const uint4*>(xc0 + (size_t)b * nb * 4 * kRegion) + h * 6;
-#pragma unroll
-              for (int pl = 0; pl < 3; ++pl) {
-                const uint4 xl = xp[2 * pl], xh = xp[2 * pl + 1];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  if (pl < 2) {
-                    lo[b][pl] = dp4a_uu(ql[k], word_of(xl, k), lo[b][pl]);
-                    hi[b][pl] = dp4a_uu(qh[k], word_of(xh, k), hi[b][pl]);
-                  } else {
-                    lo[b][pl] = dp4a_us(ql[k], word_of(xl, k), lo[b][pl]);
-                    hi[b][pl] = dp4a_us(qh[k], word_of(xh, k), hi[b][pl]);
-                  }
-                }
-              }
-            }
-          }
-          // sub-blocks 2c (low nibbles) and 2c+1 (high nibbles)
-          const uint32_t scw = c < 2 ? sc03 : sc47, mw = c < 2 ? m03 : m47;
-          const int bi = 2 * (c & 1);
-          const float sc_lo = byte_f(scw, bi), sc_hi = byte_f(scw, bi + 1);
-          const float m_lo = byte_f(mw, bi), m_hi = byte_f(mw, bi + 1);
-#pragma unroll
-          for (int b = 0; b < B; ++b) {
-            // P = 65536*P2 + (256*P1 + P0); the bracket is an exact int32
-            const float p_lo = fmaf((float)lo[b][2], 65536.0f, (float)(lo[b][1] * 256 + lo[b][0]));
-            const float p_hi = fmaf((float)hi[b][2], 65536.0f, (float)(hi[b][1] * 256 + hi[b][0]));
-            const float4 ss = *reinterpret_cast<const float4*>(xss + ((size_t)b * nb + sb) * 8 + 2 * c);
-            scaled[b] = fmaf(sc_hi * ss.z, p_hi, fmaf(sc_lo * ss.x, p_lo, scaled[b]));
-            mins[b] = fmaf(m_hi, ss.w, fmaf(m_lo, ss.y, mins[b]));
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < B; ++b) acc[b] = fmaf(dm.x, scaled[b], -dm.y * mins[b]);
+        gemv::superblock_dot<B, CPL>(p, xs, xss, nb, sb, c0, acc);
       }
       // release the stage once every lane of the warp has read it
       __syncwarp();

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+struct q4k_gemv_job;
+
 namespace q4k {
 
 constexpr int kQK = 256;         // weights per superblock
@@ -41,6 +43,13 @@ cudaError_t launch_gemv_block144(const uint8_t* const* w, const int64_t* rows, i
                                  const float* x, int batch, const float* const* residual,
                                  float* const* y, cudaStream_t s);
 bool gemv_supported(const int64_t* rows, int n_mats, int64_t cols, int batch);
+
+// Persistent GEMV over an ordered job list (q4k_gemv_seq).  Both return a
+// q4k_status; launch_gemv_seq stores the launch's CUDA error in *cuda_err.
+constexpr int kGemvSeqMaxJobs = 256;
+int gemv_seq_workspace(const q4k_gemv_job* jobs, int n_jobs, int batch, size_t* bytes);
+int launch_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int batch, void* workspace, size_t workspace_bytes,
+                    cudaStream_t s, cudaError_t* cuda_err);
 
 // Small-tile integer MMQ on CUDA cores (dp4a).  When `p_out` is non-null
 // the kernel stores the raw per-block integer dots there instead of y.

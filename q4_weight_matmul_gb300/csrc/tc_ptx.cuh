@@ -29,6 +29,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrival that counts `count` times toward the phase's expected arrivals.
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}"
+               ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

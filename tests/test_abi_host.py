@@ -86,6 +86,35 @@ def test_validation_before_any_launch(lib):
     assert lib.q4k_pack(None, None, None, None, None, 0, 256, 0, None, None) == 0
 
 
+def test_gemv_seq_validation_before_any_launch(lib):
+    import q4_weight_matmul_gb300 as q4k
+    fake, odd = 0x10000, 0x10008
+
+    def jobs(*specs):
+        arr = (q4k.GemvJob * max(1, len(specs)))()
+        for i, (rows, cols, x) in enumerate(specs):
+            arr[i].w, arr[i].rows, arr[i].cols, arr[i].x, arr[i].y = fake, rows, cols, x, fake
+        return arr
+
+    ws = ctypes.c_void_p(fake)
+    ok2 = jobs((8, 256, fake), (16, 512, fake))
+    assert lib.q4k_gemv_seq(None, 1, 0, 1, ws, 1 << 20, None) == 1          # null list
+    assert lib.q4k_gemv_seq(ok2, -1, 0, 1, ws, 1 << 20, None) == 1
+    assert lib.q4k_gemv_seq(jobs(*[(8, 256, fake)] * 257), 257, 0, 1, ws, 1 << 20, None) == 3
+    assert lib.q4k_gemv_seq(ok2, 2, 5, 1, ws, 1 << 20, None) == 3            # unknown layout
+    assert lib.q4k_gemv_seq(ok2, 2, 0, 9, ws, 1 << 20, None) == 3            # batch above 8
+    assert lib.q4k_gemv_seq(ok2, 2, 0, -1, ws, 1 << 20, None) == 1
+    assert lib.q4k_gemv_seq(jobs((8, 300, fake)), 1, 0, 1, ws, 1 << 20, None) == 1
+    assert lib.q4k_gemv_seq(jobs((8, 256, odd)), 1, 0, 1, ws, 1 << 20, None) == 2
+    assert lib.q4k_gemv_seq(ok2, 2, 0, 1, None, 1 << 20, None) == 1          # no workspace
+    assert lib.q4k_gemv_seq(ok2, 2, 0, 1, ctypes.c_void_p(odd), 1 << 20, None) == 2
+    # nothing to do: zero rows everywhere, or batch 0
+    assert lib.q4k_gemv_seq(jobs((0, 256, None)), 1, 0, 1, None, 0, None) == 0
+    assert lib.q4k_gemv_seq(ok2, 2, 0, 0, None, 0, None) == 0
+    assert lib.q4k_gemv_seq(None, 0, 0, 1, None, 0, None) == 0
+    assert lib.q4k_gemv_seq_workspace_bytes(jobs((8, 300, fake)), 1, 1) == 0
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     import q4_weight_matmul_gb300 as q4k

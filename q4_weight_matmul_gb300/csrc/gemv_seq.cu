@@ -3,44 +3,46 @@
 // Path C: the GEMVs are the hot decode kernels and every decode step streams
 // the whole model; §2: decode is bound by memory bandwidth).
 //
-// One CTA per SM stays resident for the whole list.  Its producer warp
-// streams weights into a shared-memory ring and waits for nothing but free
-// ring space, so the weight stream runs on across matrix boundaries and
-// across the dependency points between jobs; 16 consumer warps dequantise
-// and reduce.  This removes the launch gap, the start-up latency and the
-// drain that separate launches pay at every matrix boundary.
+// One CTA per SM stays resident for the whole list.  Its producer thread
+// streams weights into a shared-memory ring with 3-D tensor copies and waits
+// for nothing but a free slot, so the weight stream runs on across matrix
+// boundaries and across the dependency points between jobs; 16 consumer
+// warps dequantise and reduce.  This removes the launch gap, the start-up
+// latency and the drain that separate launches pay at every matrix boundary.
 //
-// Segments.  Consecutive jobs that read the same x (same cols) form a
-// segment.  A job with `wait` set starts a segment whose activations are read
-// only after every earlier job has completed (a grid-wide arrival counter in
-// the workspace); that is how a job consumes an earlier job's output inside
-// the launch.  Only the activation reads wait: the weights of the waiting
-// segment are already streaming into the ring.
+// Segments and epochs.  Consecutive jobs that read the same x (same cols)
+// form a segment; the segments between two jobs with `wait` set form an
+// epoch.  An epoch reads its activations only after every earlier job has
+// completed (a grid-wide arrival counter in the workspace); that is how a job
+// consumes an earlier job's output inside the launch.  Only the activation
+// reads wait: the weights of the waiting epoch are already streaming into
+// the ring.
 //
-// Work split.  A segment's rows (its jobs' rows, in order) are cut into
-// equal contiguous runs, one per CTA (+-1 row), so every SM streams the same
-// number of bytes whatever the matrix shape, and no row is shared between
-// CTAs.  Rows of one job are contiguous in memory, so a stage of up to RS
-// consecutive rows (about 24 KB, at least 8 rows) is ONE bulk copy: on GB300
-// a bulk copy costs the copy engine a roughly fixed time, and copies of a
-// few hundred bytes cannot reach the HBM rate while copies of 5 KB and more
-// do.  Stages of varying size sit in a byte ring in shared memory, allocated
-// and released in order.
+// Units.  Rows are cut into blocks of 32; a unit is one row block x two
+// superblocks (32 x 2 x 144 bytes) and is one tensor copy into one ring slot,
+// laid out [superblock][row][144] so that lane r of the consuming warp reads
+// row r without bank conflicts and all 32 lanes read the same activations
+// (broadcast).  On GB300 a tensor copy costs the copy engine a roughly fixed
+// time: boxes of 4.6 KB stream at about half the HBM rate, boxes of 9 KB and
+// more at nearly all of it.  An
+// epoch's units (its segments in order, each row-block-major) are cut into
+// equal contiguous ranges, one per CTA, so every SM streams the same number
+// of bytes whatever the matrix shapes, and a CTA stages new activations only
+// where its range enters another segment.  A row block cut by range
+// boundaries is finished by several CTAs: each stores its partial row sums in
+// the workspace and the last one to finish adds the pieces in CTA order (the
+// result does not depend on timing) and stores y.
 //
-// Consumers.  A unit is one group of 8 rows x 4 consecutive superblocks; a
-// lane takes one row's whole superblock (256 weights), the 4 lanes of a row
-// take the 4 superblocks, and the 8 rows of a warp read the same activations
-// (shared-memory broadcast).  The 16 warps take a stage's units round-robin
-// (continuing the rotation from stage to stage) and every warp visits every
-// stage in order.  Each unit leaves one partial per row; after a pass of
-// stages the CTA adds each row's partials in superblock order
-// (deterministic), adds the residual and stores y.
+// Reduction.  Consumer warps take the CTA's units round-robin; each unit
+// leaves one partial per row in shared memory, and after a pass of units the
+// CTA adds each row's partials in superblock order (deterministic).
 //
 // Arithmetic: 23-bit fixed-point activation planes and exact integer dp4a
 // block sums, scales applied in fp32 (gemv_common.cuh).
 #include "gemv_common.cuh"
 #include "q4k_internal.h"
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 #include <q4k.h>
 
@@ -53,55 +55,68 @@ namespace {
 
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = 32 * kConsumerWarps;
-constexpr int kThreads = kConsumers + 32;   // + one producer warp
-constexpr int kGroupRows = 8;               // rows of one warp unit (4 lanes per row)
-constexpr int kStageTarget = 24576;         // bytes a stage aims at
-constexpr int kMaxStageRows = 64;
-constexpr int kNumBars = 16;                // stages in flight at most
+constexpr int kThreads = kConsumers + 32;          // + one producer warp
+constexpr int kRB = 32;                            // rows per block (one per lane)
+constexpr int kUnitSB = 2;                         // superblocks per unit
+constexpr int kUnitBytes = kUnitSB * kRB * kBlockBytes;   // one ring slot
+constexpr int kMaxRing = 24;
+constexpr int kLaunchJobs = 96;                    // jobs per launch (tensor maps in the parameters)
 constexpr size_t kSyncBytes = 256;
 
 struct SeqJob {
-  const uint8_t* w;
   const float* res;
   float* y;
   int rows;
-  int row_base;     // first row of the job within its segment
+  int rb_base;      // first row block of the job within its segment
 };
 
 struct SeqSeg {
   const float* x;
+  long long unit_base;   // first unit of the segment within its epoch
   int job_begin, job_end;
-  int nb;           // superblocks per row
-  int rows;         // rows of the segment
-  int ctas;         // CTAs sharing its rows (<= grid, <= rows)
-  int stage_rows;   // rows per full stage
-  int pass_rows;    // rows per pass of partial sums
-  int wait;         // read x only after every earlier segment has completed
+  int nb;                // superblocks per row
+  int nu;                // units per row block: ceil(nb / kUnitSB)
+  int n_rb;              // row blocks of the segment
+};
+
+struct SeqEpoch {
+  long long units;       // units of all its segments
+  int seg_begin, seg_end;
+  int ctas;              // CTAs sharing its units (<= grid)
 };
 
 struct SeqParams {
-  SeqJob job[kGemvSeqMaxJobs];
-  SeqSeg seg[kGemvSeqMaxJobs];
-  int n_seg;
+  CUtensorMap map[kLaunchJobs];   // one per job: box of 144 bytes x 32 rows x 2 superblocks
+  SeqJob job[kLaunchJobs];
+  SeqSeg seg[kLaunchJobs];
+  SeqEpoch epoch[kLaunchJobs];
+  int n_epoch;
+  int ring;
   int nb_max;
   int part_floats;
-  int ring_bytes;
-  unsigned* sync;     // [0] segment arrivals, [1] CTAs exited
+  unsigned* sync;     // [0] segment arrivals, [1] CTAs exited, [2] abort
+  unsigned* tickets;  // [2][grid]: pieces of a split row block stored (epoch parity)
+  float* pieces;      // [2][grid][2][kRB * B]: a CTA's first / last row block
   int* err;
 };
 
+// kernel parameters are limited to 32764 bytes
+static_assert(sizeof(SeqParams) <= 32000, "too many jobs per launch for the kernel parameter space");
+
 struct SeqLayout {
-  size_t xs, xss, part, ring, bars, total;
+  size_t xs, xss, part, carry, flags, ring, bars, total;
 };
 
-__host__ __device__ inline SeqLayout seq_layout(int B, int nb_max, int part_floats, int ring_bytes) {
+__host__ __device__ inline SeqLayout seq_layout(int B, int nb_max, int part_floats, int ring) {
   SeqLayout L;
   L.xs = 0;
   L.xss = L.xs + gemv::xs_bytes(B, nb_max);
   L.part = L.xss + gemv::xss_bytes(B, nb_max);
-  L.ring = (L.part + sizeof(float) * (size_t)part_floats + 127) & ~size_t(127);
-  L.bars = L.ring + (size_t)ring_bytes;
-  L.total = L.bars + sizeof(uint64_t) * 2 * kNumBars + 16 + 1024;   // + flags, + base alignment slack
+  L.carry = L.part + sizeof(float) * (size_t)part_floats;
+  L.flags = L.carry + sizeof(float) * 2 * kRB * (size_t)B;
+  L.ring = (L.flags + 16 + 127) & ~size_t(127);
+  L.bars = L.ring + (size_t)ring * kUnitBytes;
+  L.total = L.bars + sizeof(uint64_t) * 2 * ring + 16 + 1024;   // + issue counter, + base alignment slack
   return L;
 }
 
@@ -119,6 +134,17 @@ __device__ __forceinline__ void red_release_add_gpu(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ unsigned atom_acq_rel_add_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void record_failure(const SeqParams& P) {
+  atomicOr(P.err, 2);
+  atomicExch(P.sync + 2, 1u);
+}
+
 // Bounded wait until `target` segment arrivals have been counted.
 __device__ __noinline__ bool grid_wait(const unsigned* counter, unsigned target) {
   if (ld_acquire_gpu(counter) >= target) return true;
@@ -130,117 +156,143 @@ __device__ __noinline__ bool grid_wait(const unsigned* counter, unsigned target)
   return true;
 }
 
-// The contiguous run of the segment's rows that CTA c owns.
-__device__ __forceinline__ void cta_rows(const SeqSeg& S, int c, int& r0, int& r1) {
-  if (c >= S.ctas) {
-    r0 = r1 = 0;
-    return;
-  }
-  r0 = (int)((long long)c * S.rows / S.ctas);
-  r1 = (int)((long long)(c + 1) * S.rows / S.ctas);
+// First unit of CTA c's range in epoch E (c = ctas gives the end).
+__device__ __forceinline__ long long range_begin(const SeqEpoch& E, int c) {
+  return (long long)c * E.units / E.ctas;
 }
 
-__device__ __forceinline__ int job_of_row(const SeqParams& P, const SeqSeg& S, int r) {
+// The CTA whose range holds epoch unit u.
+__device__ __forceinline__ int owner_of(const SeqEpoch& E, long long u) {
+  return (int)(((u + 1) * E.ctas + E.units - 1) / E.units - 1);
+}
+
+__device__ __forceinline__ int job_of(const SeqParams& P, const SeqSeg& S, long long rb) {
   int j = S.job_begin;
-  while (j + 1 < S.job_end && r >= P.job[j + 1].row_base) ++j;
+  while (j + 1 < S.job_end && rb >= P.job[j + 1].rb_base) ++j;
   return j;
 }
 
-// The stage that starts at segment row r (< r1): its job and row count.
-__device__ __forceinline__ int stage_at(const SeqParams& P, const SeqSeg& S, int r, int r1, int& jb) {
-  jb = job_of_row(P, S, r);
-  const SeqJob& J = P.job[jb];
-  return min(S.stage_rows, min(r1, J.row_base + J.rows) - r);
+// Piece held by CTA c of the row block whose units are epoch units
+// [f, f + nu): side 0 if it is c's first row block, else side 1.
+__device__ __forceinline__ float* piece_of(const SeqParams& P, const SeqEpoch& E, int slot, int grid, int c,
+                                           long long f, int nu, int B) {
+  const long long u0 = range_begin(E, c);
+  const int side = (u0 >= f && u0 < f + nu) ? 0 : 1;
+  return P.pieces + (((size_t)slot * grid + c) * 2 + side) * (size_t)(kRB * B);
 }
 
-// Byte position of the next stage in the ring: stages never wrap.
-__device__ __forceinline__ uint32_t ring_place(uint32_t head, uint32_t bytes, uint32_t ring_bytes) {
-  return head + bytes > ring_bytes ? 0u : head;
-}
-
-__device__ __forceinline__ void record_failure(const SeqParams& P) { atomicOr(P.err, 2); }
-
-// Units of one stage for this warp: unit u is row group u / ng (8 rows) x
-// superblock group u % ng (4 superblocks, ng = ceil(nb / 4)), and belongs to
-// warp (base + u) % 16.  Lane (r, q) = (lane / 4, lane % 4) takes row r of
-// the group and superblock 4*(u % ng) + q whole; the 4 lanes of a row add
-// their superblocks ((s0 + s1) + (s2 + s3)) and lane q = 0 stores one
-// partial per row and superblock group: part[row][group][b].
+// Consumer warps over slots [ps, pe) of a run of one segment's units: slot s
+// is segment unit u0 + s and stage J + s.  Each unit leaves 32 partial row
+// sums (its two superblocks added in order) in part[s - ps][row][b].
 template <int B>
-__device__ __forceinline__ void consume_stage(const uint8_t* stage, int n_rows, int nb, int base, float* part,
-                                              int pass_row, const uint8_t* xs, const float2* xss, int warp,
-                                              int lane) {
-  const int ng = (nb + 3) >> 2;
-  const int n_units = ((n_rows + kGroupRows - 1) / kGroupRows) * ng;
-  const int r_in = lane >> 2, q = lane & 3;
-  int u = (warp - base % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-  int g = u / ng, sg = u - g * ng;
-  for (; u < n_units; u += kConsumerWarps) {
-    const int row = g * kGroupRows + r_in, sb = sg * 4 + q;
+__device__ __forceinline__ void consume_pass(const SeqParams& P, const uint8_t* ring_base, uint64_t* full,
+                                             uint64_t* empty, volatile int* issued, int ring, int J, int ps,
+                                             int pe, long long u0, int nb, int nu, const uint8_t* xs,
+                                             const float2* xss, float* part, bool& ok, int warp, int lane) {
+  for (int s = ps + warp; s < pe; s += kConsumerWarps) {
+    const int j = J + s;
+    const int slot = j % ring;
+    const uint32_t parity = (uint32_t)((j / ring) & 1);
+    // a warp that skips stages must see stage j issued before it waits on
+    // its parity (the copy of stage j - ring may still be in flight)
+    if (ok && *issued <= j && !gemv::wait_issued(issued, j)) {
+      ok = false;
+      if (lane == 0) record_failure(P);
+    }
+    if (ok && !tc::mbar_wait_spin(&full[slot], parity)) {
+      ok = false;
+      if (lane == 0) record_failure(P);
+    }
     float acc[B];
 #pragma unroll
     for (int b = 0; b < B; ++b) acc[b] = 0.0f;
-    if (row < n_rows && sb < nb)
-      gemv::superblock_dot<B, 4>(stage + ((size_t)row * nb + sb) * kBlockBytes, xs, xss, nb, sb, 0, acc);
+    if (ok) {
+      const int sb = (int)((u0 + s) % nu) * kUnitSB;
+      const uint8_t* p = ring_base + (size_t)slot * kUnitBytes + lane * kBlockBytes;
+      gemv::superblock_dot<B, 4>(p, xs, xss, nb, sb, 0, acc);
+      if (sb + 1 < nb) {
+        float acc2[B];
+        gemv::superblock_dot<B, 4>(p + kRB * kBlockBytes, xs, xss, nb, sb + 1, 0, acc2);
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-      acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 1);
-      acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 2);
+        for (int b = 0; b < B; ++b) acc[b] += acc2[b];
+      }
     }
-    if (q == 0 && row < n_rows) {
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&empty[slot]);
 #pragma unroll
-      for (int b = 0; b < B; ++b) part[((size_t)(pass_row + row) * ng + sg) * B + b] = acc[b];
-    }
-    // next unit of this warp: 16 units on
-    sg += kConsumerWarps;
-    while (sg >= ng) {
-      sg -= ng;
-      ++g;
-    }
+    for (int b = 0; b < B; ++b) part[((size_t)(s - ps) * kRB + lane) * B + b] = acc[b];
   }
 }
 
-// Rows [pr0, pr0 + n) of the segment, partials part[row - pr0][group][b]:
-// y = sum over superblock groups in order (+ residual).
+// Row sums of the segment units [ua, ub) of this pass, where [u0, u1) is the
+// CTA's part of the segment, in superblock order.  A row block whose part
+// continues into the next pass leaves its sum in carry_out; one that began
+// in the previous pass starts from carry_in.  A row block finished here is
+// stored to y, or, if the CTA's range cuts it, to this CTA's piece of it.
 template <int B>
-__device__ __forceinline__ void reduce_pass(const SeqParams& P, const SeqSeg& S, int pr0, int n, const float* part,
-                                            int tid) {
-  const int ng = (S.nb + 3) >> 2;
-  for (int i = tid; i < n * B; i += kConsumers) {
-    const int rr = i / B, b = i - rr * B;
-    const int r = pr0 + rr;
-    const SeqJob& J = P.job[job_of_row(P, S, r)];
-    const int row = r - J.row_base;
-    const float* pp = part + (size_t)rr * ng * B + b;
-    float v = 0.0f;
-    for (int k = 0; k < ng; ++k) v += pp[(size_t)k * B];
-    if (J.res) v += __ldcg(J.res + (size_t)b * J.rows + row);
-    J.y[(size_t)b * J.rows + row] = v;
+__device__ __forceinline__ void reduce_pass(const SeqParams& P, const SeqSeg& S, const SeqEpoch& E, int slot,
+                                            long long u0, long long u1, long long ua, long long ub,
+                                            const float* part, const float* carry_in, float* carry_out, int c,
+                                            int grid, int tid) {
+  const int nu = S.nu;   // units per row block
+  const long long rb_lo = ua / nu, rb_hi = (ub - 1) / nu;
+  const int n_rbp = (int)(rb_hi - rb_lo + 1);
+  constexpr int per = kRB * B;
+  for (int i = tid; i < n_rbp * per; i += kConsumers) {
+    const int k = i / per, rem = i - k * per, r = rem / B, b = rem - r * B;
+    const long long rb = rb_lo + k;
+    const long long first = rb * nu, last = first + nu;
+    const long long a = first > ua ? first : ua, e = last < ub ? last : ub;
+    float v = ((first > u0 ? first : u0) < ua) ? carry_in[rem] : 0.0f;
+    for (long long uu = a; uu < e; ++uu) v += part[((uu - ua) * kRB + r) * B + b];
+    if ((last < u1 ? last : u1) > ub) {
+      carry_out[rem] = v;
+      continue;
+    }
+    if (first < u0 || last > u1) {
+      piece_of(P, E, slot, grid, c, S.unit_base + first, nu, B)[rem] = v;
+      continue;
+    }
+    const SeqJob& Jb = P.job[job_of(P, S, rb)];
+    const long long row = (rb - Jb.rb_base) * kRB + r;
+    if (row >= Jb.rows) continue;
+    if (Jb.res) v += __ldcg(Jb.res + (size_t)b * Jb.rows + row);
+    Jb.y[(size_t)b * Jb.rows + row] = v;
   }
+}
+
+// The segment of epoch E that holds epoch unit u.
+__device__ __forceinline__ int seg_of(const SeqParams& P, const SeqEpoch& E, long long u) {
+  int s = E.seg_begin;
+  while (s + 1 < E.seg_end && u >= P.seg[s + 1].unit_base) ++s;
+  return s;
 }
 
 template <int B>
 __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_constant__ SeqParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  const SeqLayout L = seq_layout(B, P.nb_max, P.part_floats, P.ring_bytes);
+  const int ring = P.ring;
+  const SeqLayout L = seq_layout(B, P.nb_max, P.part_floats, ring);
   uint8_t* xs = smem + L.xs;
   float2* xss = reinterpret_cast<float2*>(smem + L.xss);
   float* part = reinterpret_cast<float*>(smem + L.part);
-  uint8_t* ring = smem + L.ring;
+  float* carry = reinterpret_cast<float*>(smem + L.carry);
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + L.flags);
+  uint8_t* ring_base = smem + L.ring;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + kNumBars;
-  volatile int* flags = reinterpret_cast<volatile int*>(empty + kNumBars);
+  uint64_t* empty = full + ring;
+  volatile int* issued = reinterpret_cast<volatile int*>(empty + ring);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, grid = gridDim.x;
-  const uint32_t ring_bytes = (uint32_t)P.ring_bytes;
 
   if (tid == 0) {
-    for (int i = 0; i < kNumBars; ++i) {
+    for (int i = 0; i < ring; ++i) {
       tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], kConsumerWarps);
+      tc::mbar_init(&empty[i], 1);
     }
-    flags[0] = 0;
+    *issued = 0;
+    flags[0] = flags[1] = flags[2] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -248,54 +300,51 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      // in-flight stages [oldest, j); stage k occupies [pos_k, end_k) of the ring
-      uint32_t spos[kNumBars], send[kNumBars];
-      int j = 0, oldest = 0;
-      uint32_t head = 0;
-      bool ok = true;
-      for (int si = 0; si < P.n_seg && ok; ++si) {
-        const SeqSeg& S = P.seg[si];
-        int r0, r1;
-        cta_rows(S, c, r0, r1);
-        const size_t row_bytes = (size_t)S.nb * kBlockBytes;
-        for (int r = r0; r < r1 && ok;) {
-          int jb;
-          const int n = stage_at(P, S, r, r1, jb);
-          const uint32_t bytes = (uint32_t)(n * row_bytes);
-          const uint32_t pos = ring_place(head, bytes, ring_bytes);
-          // release stages in order until none in flight overlaps the new
-          // stage's bytes (after a wrap to 0 the oldest stage may lie in the
-          // skipped tail while a younger one overlaps) and a barrier is free
-          while (oldest < j) {
-            bool busy = j - oldest >= kNumBars;
-            for (int k = oldest; k < j && !busy; ++k)
-              busy = pos < send[k % kNumBars] && spos[k % kNumBars] < pos + bytes;
-            if (!busy) break;
-            if (!tc::mbar_wait_sleep(&empty[oldest % kNumBars], (uint32_t)((oldest / kNumBars) & 1))) {
-              ok = false;
+      int j = 0, slot = 0;
+      uint32_t phase = 0;
+      bool pok = true;
+      for (int ei = 0; ei < P.n_epoch && pok; ++ei) {
+        const SeqEpoch& E = P.epoch[ei];
+        if (c >= E.ctas) continue;
+        const long long e1 = range_begin(E, c + 1);
+        long long u = range_begin(E, c);
+        int si = seg_of(P, E, u);
+        while (u < e1 && pok) {
+          const SeqSeg& S = P.seg[si];
+          const int nu = S.nu;
+          const long long su1 = S.unit_base + (long long)S.n_rb * nu;
+          const long long end = e1 < su1 ? e1 : su1;
+          long long rb = (u - S.unit_base) / nu;
+          int up = (int)(u - S.unit_base - rb * nu);
+          int jb = job_of(P, S, rb);
+          for (; u < end; ++u) {
+            if (!tc::mbar_wait_spin(&empty[slot], phase ^ 1)) {
+              record_failure(P);
+              pok = false;
               break;
             }
-            ++oldest;
+            tc::mbar_arrive_expect_tx(&full[slot], kUnitBytes);
+            tc::tma_load_3d(ring_base + (size_t)slot * kUnitBytes, &P.map[jb], 0,
+                            (int)(rb - P.job[jb].rb_base) * kRB, up * kUnitSB, &full[slot]);
+            __threadfence_block();
+            *issued = ++j;
+            if (++slot == ring) {
+              slot = 0;
+              phase ^= 1;
+            }
+            if (++up == nu) {
+              up = 0;
+              ++rb;
+              if (jb + 1 < S.job_end && rb >= P.job[jb + 1].rb_base) ++jb;
+            }
           }
-          if (!ok) {
-            record_failure(P);
-            break;
-          }
-          const int slot = j % kNumBars;
-          spos[slot] = pos;
-          send[slot] = pos + bytes;
-          const SeqJob& J = P.job[jb];
-          tc::mbar_arrive_expect_tx(&full[slot], bytes);
-          tc::bulk_g2s(ring + pos, J.w + (size_t)(r - J.row_base) * row_bytes, bytes, &full[slot]);
-          head = pos + bytes;
-          ++j;
-          r += n;
+          ++si;
         }
       }
       // every copy issued has landed before the CTA exits, even if consumers
       // gave up a wait and left early (bounded as well)
-      for (int k = max(oldest, j - kNumBars); k < j; ++k)
-        if (!tc::mbar_wait_sleep(&full[k % kNumBars], (uint32_t)((k / kNumBars) & 1))) record_failure(P);
+      for (int k = max(0, j - ring); k < j; ++k)
+        if (!tc::mbar_wait_sleep(&full[k % ring], (uint32_t)((k / ring) & 1))) record_failure(P);
     }
     return;
   }
@@ -304,76 +353,114 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
   bool ok = true;
   const float* staged_x = nullptr;
   int staged_nb = -1;
-  int j = 0;            // stage index in this CTA's ring order
-  uint32_t head = 0;    // ring position, replayed exactly as the producer places stages
-  int unit_base = 0;    // rotation of units over warps
-  for (int si = 0; si < P.n_seg; ++si) {
-    const SeqSeg& S = P.seg[si];
-    int r0, r1;
-    cta_rows(S, c, r0, r1);
-    const int nb = S.nb;
-    const size_t row_bytes = (size_t)nb * kBlockBytes;
-    if (S.wait) {
+  int J = 0;          // this CTA's stages so far (ring order)
+  int pass_no = 0;
+  constexpr int per = kRB * B;
+  for (int ei = 0; ei < P.n_epoch; ++ei) {
+    const SeqEpoch& E = P.epoch[ei];
+    const int slot = ei & 1;
+    long long e0 = 0, e1 = 0;
+    if (c < E.ctas) {
+      e0 = range_begin(E, c);
+      e1 = range_begin(E, c + 1);
+    }
+    if (ei > 0) {
       // activations may be outputs of earlier jobs: wait for all of them
-      if (tid == 0 && ok && !grid_wait(P.sync, (unsigned)si * (unsigned)grid)) {
+      if (tid == 0 && ok && !grid_wait(P.sync, (unsigned)ei * (unsigned)grid)) {
         record_failure(P);
-        flags[0] = 1;
+        flags[2] = 1;
       }
       named_sync_consumers();
-      ok = ok && !flags[0];
+      ok = ok && !flags[2];
+      staged_x = nullptr;
     }
-    if (r1 > r0) {
-      if (S.wait || S.x != staged_x || nb != staged_nb) {
-        if (ok) gemv::stage_x<B, kConsumers, true>(S.x, nb, xs, xss, tid);
+    for (long long u = e0; u < e1;) {
+      const int si = seg_of(P, E, u);
+      const SeqSeg& S = P.seg[si];
+      const int nb = S.nb, nu = S.nu;
+      const long long su1 = S.unit_base + (long long)S.n_rb * nu;
+      const long long u0 = u - S.unit_base, u1 = (e1 < su1 ? e1 : su1) - S.unit_base;   // segment units
+      const int n_units = (int)(u1 - u0);
+      if (S.x != staged_x || nb != staged_nb) {
+        gemv::stage_x<B, kConsumers, true>(S.x, nb, xs, xss, tid);
         staged_x = S.x;
         staged_nb = nb;
         named_sync_consumers();
       }
-      int pass_r0 = r0, pass_n = 0;
-      for (int r = r0; r < r1;) {
-        int jb;
-        const int n = stage_at(P, S, r, r1, jb);
-        if (pass_n + n > S.pass_rows) {
-          // partials of the pass are complete: reduce them
-          if (!ok) flags[0] = 1;
-          named_sync_consumers();
-          ok = ok && !flags[0];
-          if (ok) reduce_pass<B>(P, S, pass_r0, pass_n, part, tid);
-          named_sync_consumers();
-          pass_r0 = r;
-          pass_n = 0;
-        }
-        const uint32_t bytes = (uint32_t)(n * row_bytes);
-        const uint32_t pos = ring_place(head, bytes, ring_bytes);
-        const int slot = j % kNumBars;
-        if (ok && !tc::mbar_wait_sleep(&full[slot], (uint32_t)((j / kNumBars) & 1))) {
-          ok = false;
-          if (lane == 0) record_failure(P);
-        }
-        if (ok) consume_stage<B>(ring + pos, n, nb, unit_base, part, pass_n, xs, xss, warp, lane);
-        // every warp releases every stage once, after its lanes read it
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&empty[slot]);
-        unit_base += ((n + kGroupRows - 1) / kGroupRows) * ((nb + 3) >> 2);
-        head = pos + bytes;
-        ++j;
-        pass_n += n;
-        r += n;
+      const int pu = P.part_floats / per;   // units per pass, a multiple of 16
+      for (int ps = 0; ps < n_units; ps += pu, ++pass_no) {
+        const int pe = min(ps + pu, n_units);
+        consume_pass<B>(P, ring_base, full, empty, issued, ring, J, ps, pe, u0, nb, nu, xs, xss, part, ok, warp,
+                        lane);
+        if (!ok) flags[2] = 1;
+        named_sync_consumers();
+        ok = ok && !flags[2];
+        if (ok)
+          reduce_pass<B>(P, S, E, slot, u0, u1, u0 + ps, u0 + pe, part, carry + (pass_no & 1) * per,
+                         carry + ((pass_no + 1) & 1) * per, c, grid, tid);
+        named_sync_consumers();
       }
-      if (!ok) flags[0] = 1;
-      named_sync_consumers();
-      ok = ok && !flags[0];
-      if (ok) reduce_pass<B>(P, S, pass_r0, pass_n, part, tid);
+      J += n_units;
+      u += n_units;
     }
-    // every output of this CTA for the segment is stored: count the arrival
+    if (e1 > e0 && ok) {
+      // row blocks cut by this CTA's range: the last holder adds the pieces
+      const int s_first = seg_of(P, E, e0), s_last = seg_of(P, E, e1 - 1);
+      const SeqSeg& Sf = P.seg[s_first];
+      const SeqSeg& Sl = P.seg[s_last];
+      const long long f_first = Sf.unit_base + (e0 - Sf.unit_base) / Sf.nu * Sf.nu;   // first unit of the row block
+      const long long f_last = Sl.unit_base + (e1 - 1 - Sl.unit_base) / Sl.nu * Sl.nu;
+      const bool split_first = f_first < e0 || f_first + Sf.nu > e1;
+      const bool split_last = f_last != f_first && f_last + Sl.nu > e1;
+      if (split_first || split_last) {
+        if (tid < 2) {
+          const bool mine = tid == 0 ? split_first : split_last;
+          int fl = 0;
+          if (mine) {
+            const long long f = tid == 0 ? f_first : f_last;
+            const int nbs = tid == 0 ? Sf.nu : Sl.nu;
+            const int c0 = owner_of(E, f), c1 = owner_of(E, f + nbs - 1);
+            unsigned* t = P.tickets + (size_t)slot * grid + c1;
+            if (atom_acq_rel_add_gpu(t, 1u) == (unsigned)(c1 - c0)) {
+              fl = 1;
+              atomicExch(t, 0u);
+            }
+          }
+          flags[tid] = fl;
+        }
+        named_sync_consumers();
+        const int fl = flags[0] | (flags[1] << 1);
+        for (int i = tid; i < 2 * per; i += kConsumers) {
+          const int side = i / per, rem = i - side * per;
+          if (!(fl & (1 << side))) continue;
+          const SeqSeg& S = side == 0 ? Sf : Sl;
+          const long long f = side == 0 ? f_first : f_last;
+          const long long rb = (f - S.unit_base) / S.nu;
+          const int r = rem / B, b = rem - r * B;
+          const SeqJob& Jb = P.job[job_of(P, S, rb)];
+          const long long row = (rb - Jb.rb_base) * kRB + r;
+          if (row >= Jb.rows) continue;
+          const int c0 = owner_of(E, f), c1 = owner_of(E, f + S.nu - 1);
+          float v = 0.0f;
+          for (int cc = c0; cc <= c1; ++cc) v += __ldcg(piece_of(P, E, slot, grid, cc, f, S.nu, B) + rem);
+          if (Jb.res) v += __ldcg(Jb.res + (size_t)b * Jb.rows + row);
+          Jb.y[(size_t)b * Jb.rows + row] = v;
+        }
+      }
+    }
+    // every output of this CTA for the epoch is stored: count the arrival
     named_sync_consumers();
     if (tid == 0) red_release_add_gpu(P.sync, 1u);
   }
 
-  // the last CTA out resets the counters for the next launch
+  // the last CTA out resets the workspace for the next launch
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(P.sync + 1, 1u) == (unsigned)grid - 1) {
+      if (atomicAdd(P.sync + 2, 0u) != 0u) {
+        for (int i = 0; i < 2 * grid; ++i) P.tickets[i] = 0u;
+        P.sync[2] = 0u;
+      }
       atomicExch(P.sync, 0u);
       atomicExch(P.sync + 1, 0u);
       __threadfence();
@@ -382,20 +469,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
 }
 
 struct SeqPlan {
-  int n_seg, nb_max, part_floats, ring_bytes, grid;
-  size_t smem;
+  int n_seg, n_epoch, nb_max, ring, part_floats, grid;
+  size_t smem, ws_bytes, tickets_off, pieces_off;
 };
 
-// Segments, CTA shares, stage and pass sizes of a job list.  Returns Q4K_OK or
-// a status; fills P (if not null) and the plan.
-int plan_seq(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& info, SeqParams* P,
-             SeqPlan* plan) {
-  if (n_jobs < 0 || n_jobs > kGemvSeqMaxJobs) return Q4K_ERR_UNSUPPORTED;
+// Segments, epochs, row blocks and CTA shares of one launch's jobs (at most
+// kLaunchJobs).  Fills P (if not null) and the plan; returns a status.
+int plan_launch(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& info, SeqParams* P,
+                SeqPlan* plan) {
   SeqPlan p{};
   p.grid = info.sm_count;
-  int n_seg = 0, n_job = 0;
-  SeqSeg tseg[kGemvSeqMaxJobs];
-  SeqJob tjob[kGemvSeqMaxJobs];
+  int n_seg = 0, n_job = 0, n_epoch = 0;
+  SeqSeg tseg[kLaunchJobs];
+  SeqJob tjob[kLaunchJobs];
+  SeqEpoch tep[kLaunchJobs];
+  const void* tw[kLaunchJobs];
+  int64_t tcols[kLaunchJobs];
   bool pending_wait = false;
   const float* cur_x = nullptr;
   int cur_nb = -1;
@@ -406,66 +495,88 @@ int plan_seq(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& info
     const int nb = (int)(q.cols / kQK);
     if (n_seg == 0 || pending_wait || q.x != cur_x || nb != cur_nb) {
       if (n_seg > 0) tseg[n_seg - 1].job_end = n_job;
-      SeqSeg s{};
-      s.x = q.x;
-      s.job_begin = n_job;
-      s.nb = nb;
-      s.wait = (pending_wait && n_seg > 0) ? 1 : 0;
-      tseg[n_seg++] = s;
+      if (n_seg == 0 || pending_wait) {
+        if (n_epoch > 0) tep[n_epoch - 1].seg_end = n_seg;
+        SeqEpoch e{};
+        e.seg_begin = n_seg;
+        tep[n_epoch++] = e;
+      }
+      SeqSeg sg{};
+      sg.x = q.x;
+      sg.job_begin = n_job;
+      sg.nb = nb;
+      tseg[n_seg++] = sg;
       cur_x = q.x;
       cur_nb = nb;
       pending_wait = false;
     }
     SeqJob jb{};
-    jb.w = static_cast<const uint8_t*>(q.w);
     jb.res = q.residual;
     jb.y = q.y;
     jb.rows = (int)q.rows;
+    tw[n_job] = q.w;
+    tcols[n_job] = q.cols;
     tjob[n_job++] = jb;
   }
   if (n_seg > 0) tseg[n_seg - 1].job_end = n_job;
+  if (n_epoch > 0) tep[n_epoch - 1].seg_end = n_seg;
   p.n_seg = n_seg;
+  p.n_epoch = n_epoch;
   p.nb_max = 1;
-  size_t max_stage = 0;
-  int min_part = 0;   // floats of the largest stage's partial sums
-  for (int s = 0; s < n_seg; ++s) {
-    SeqSeg& S = tseg[s];
-    int64_t rows = 0;
-    for (int j = S.job_begin; j < S.job_end; ++j) {
-      tjob[j].row_base = (int)rows;
-      rows += tjob[j].rows;
+  for (int e = 0; e < n_epoch; ++e) {
+    SeqEpoch& E = tep[e];
+    int64_t units = 0;
+    for (int s = E.seg_begin; s < E.seg_end; ++s) {
+      SeqSeg& S = tseg[s];
+      int64_t n_rb = 0;
+      for (int j = S.job_begin; j < S.job_end; ++j) {
+        tjob[j].rb_base = (int)n_rb;
+        n_rb += (tjob[j].rows + kRB - 1) / kRB;
+      }
+      S.n_rb = (int)n_rb;
+      S.nu = (S.nb + kUnitSB - 1) / kUnitSB;
+      S.unit_base = units;
+      units += n_rb * S.nu;
+      p.nb_max = std::max(p.nb_max, S.nb);
     }
-    if (rows > (int64_t(1) << 30)) return Q4K_ERR_UNSUPPORTED;
-    S.rows = (int)rows;
-    S.ctas = (int)std::min<int64_t>(p.grid, rows);
-    const int row_bytes = S.nb * kBlockBytes;
-    const int rs = (kStageTarget / row_bytes) / kGroupRows * kGroupRows;
-    S.stage_rows = std::max(kGroupRows, std::min(kMaxStageRows, rs));
-    p.nb_max = std::max(p.nb_max, S.nb);
-    max_stage = std::max(max_stage, (size_t)S.stage_rows * row_bytes);
-    min_part = std::max(min_part, S.stage_rows * ((S.nb + 3) / 4) * B);
+    if (units / p.grid > (int64_t(1) << 30)) return Q4K_ERR_UNSUPPORTED;
+    E.units = units;
+    E.ctas = (int)std::min<int64_t>(p.grid, units);
   }
-  // shared memory: staged activations, then partial sums (up to a target,
-  // at least one stage's worth), then a ring that holds two largest stages
-  const size_t fixed = seq_layout(B, p.nb_max, 0, 0).total;
-  if (fixed + 2 * max_stage + sizeof(float) * (size_t)min_part > (size_t)info.max_smem_optin)
-    return Q4K_ERR_UNSUPPORTED;
-  const size_t spare = (size_t)info.max_smem_optin - fixed - 2 * max_stage;
-  const int target = B <= 2 ? 4096 : 8192;
-  p.part_floats = (int)std::min<size_t>(target, spare / sizeof(float)) & ~31;
-  if (p.part_floats < min_part) return Q4K_ERR_UNSUPPORTED;
-  for (int s = 0; s < n_seg; ++s) tseg[s].pass_rows = p.part_floats / (((tseg[s].nb + 3) / 4) * B);
-  const size_t with_part = seq_layout(B, p.nb_max, p.part_floats, 0).total;
-  p.ring_bytes = (int)(((size_t)info.max_smem_optin - with_part) & ~size_t(127));
-  p.smem = seq_layout(B, p.nb_max, p.part_floats, p.ring_bytes).total;
-  if (p.smem > (size_t)info.max_smem_optin || (size_t)p.ring_bytes < 2 * max_stage) return Q4K_ERR_UNSUPPORTED;
+  // shared memory: activations, partial sums, then the deepest ring that fits
+  p.part_floats = 16 * kRB * B * (B <= 2 ? 8 : (B <= 4 ? 2 : 1));
+  p.ring = 0;
+  for (int ring = kMaxRing; ring >= 4; --ring) {
+    const size_t total = seq_layout(B, p.nb_max, p.part_floats, ring).total;
+    if (total <= (size_t)info.max_smem_optin) {
+      p.ring = ring;
+      p.smem = total;
+      break;
+    }
+  }
+  if (p.ring == 0) return Q4K_ERR_UNSUPPORTED;
+  // workspace: counters, then per epoch parity one ticket and two pieces per CTA
+  const size_t tickets_bytes = ((sizeof(unsigned) * 2 * (size_t)p.grid) + 255) & ~size_t(255);
+  p.tickets_off = kSyncBytes;
+  p.pieces_off = kSyncBytes + tickets_bytes;
+  p.ws_bytes = p.pieces_off + sizeof(float) * 2 * (size_t)p.grid * 2 * kRB * B;
   if (P) {
+    for (int j = 0; j < n_job; ++j) {
+      // box: a superblock's 144 bytes x 32 rows x 2 superblocks; rows and
+      // superblocks past the matrix read as zeros
+      const uint64_t nbj = (uint64_t)(tcols[j] / kQK);
+      const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)tjob[j].rows, nbj};
+      const uint64_t strides[2] = {nbj * kBlockBytes, (uint64_t)kBlockBytes};
+      const uint32_t box[3] = {(uint32_t)kBlockBytes, (uint32_t)kRB, (uint32_t)kUnitSB};
+      if (!encode_tmap_u8_3d(&P->map[j], tw[j], dims, strides, box)) return Q4K_ERR_CUDA;
+    }
     std::memcpy(P->seg, tseg, sizeof(SeqSeg) * n_seg);
     std::memcpy(P->job, tjob, sizeof(SeqJob) * n_job);
-    P->n_seg = n_seg;
+    std::memcpy(P->epoch, tep, sizeof(SeqEpoch) * n_epoch);
+    P->n_epoch = n_epoch;
+    P->ring = p.ring;
     P->nb_max = p.nb_max;
     P->part_floats = p.part_floats;
-    P->ring_bytes = p.ring_bytes;
   }
   *plan = p;
   return Q4K_OK;
@@ -496,15 +607,24 @@ cudaError_t launch_seq_b(const SeqParams& P, const SeqPlan& p, int dev, const De
   return cudaLaunchKernelEx(&cfg, gemv_seq_kernel<B>, P);
 }
 
+// Launches of a job list: consecutive chunks of at most kLaunchJobs jobs
+// (stream order between launches is a full dependency).
+int next_chunk(int i0, int n_jobs) { return std::min(n_jobs, i0 + kLaunchJobs); }
+
 }  // namespace
 
 int gemv_seq_workspace(const q4k_gemv_job* jobs, int n_jobs, int batch, size_t* bytes) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return Q4K_ERR_CUDA;
-  SeqPlan p;
-  const int st = plan_seq(jobs, n_jobs, batch, device_info(dev), nullptr, &p);
-  if (st != Q4K_OK) return st;
-  *bytes = kSyncBytes;
+  const DeviceInfo& info = device_info(dev);
+  size_t need = kSyncBytes;
+  for (int i0 = 0; i0 < n_jobs; i0 = next_chunk(i0, n_jobs)) {
+    SeqPlan p;
+    const int st = plan_launch(jobs + i0, next_chunk(i0, n_jobs) - i0, batch, info, nullptr, &p);
+    if (st != Q4K_OK) return st;
+    need = std::max(need, p.ws_bytes);
+  }
+  *bytes = need;
   return Q4K_OK;
 }
 
@@ -514,33 +634,51 @@ int launch_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int batch, void* works
   int dev = 0;
   if ((*cuda_err = cudaGetDevice(&dev)) != cudaSuccess) return Q4K_ERR_CUDA;
   const DeviceInfo& info = device_info(dev);
-  static thread_local SeqParams P;
-  std::memset(&P, 0, sizeof(P));
-  SeqPlan p;
-  const int st = plan_seq(jobs, n_jobs, batch, info, &P, &p);
-  if (st != Q4K_OK) return st;
-  if (p.n_seg == 0) return Q4K_OK;
-  if (workspace_bytes < kSyncBytes) return Q4K_ERR_INVALID_ARG;
-  P.sync = static_cast<unsigned*>(workspace);
-  P.err = device_error_word();
-  if (!P.err) {
+  int* err = device_error_word();
+  if (!err) {
     *cuda_err = cudaGetLastError();
     return Q4K_ERR_CUDA;
   }
-  cudaError_t e;
-  switch (batch) {
-    case 1: e = launch_seq_b<1>(P, p, dev, info, s); break;
-    case 2: e = launch_seq_b<2>(P, p, dev, info, s); break;
-    case 3: e = launch_seq_b<3>(P, p, dev, info, s); break;
-    case 4: e = launch_seq_b<4>(P, p, dev, info, s); break;
-    case 5: e = launch_seq_b<5>(P, p, dev, info, s); break;
-    case 6: e = launch_seq_b<6>(P, p, dev, info, s); break;
-    case 7: e = launch_seq_b<7>(P, p, dev, info, s); break;
-    case 8: e = launch_seq_b<8>(P, p, dev, info, s); break;
-    default: return Q4K_ERR_UNSUPPORTED;
+  // plan every launch before enqueuing any, so that a refused request
+  // enqueues nothing
+  size_t need = kSyncBytes;
+  for (int i0 = 0; i0 < n_jobs; i0 = next_chunk(i0, n_jobs)) {
+    SeqPlan p;
+    const int st = plan_launch(jobs + i0, next_chunk(i0, n_jobs) - i0, batch, info, nullptr, &p);
+    if (st != Q4K_OK) return st;
+    need = std::max(need, p.ws_bytes);
   }
-  *cuda_err = e;
-  return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
+  if (workspace_bytes < need) return Q4K_ERR_INVALID_ARG;
+  static thread_local SeqParams P;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  for (int i0 = 0; i0 < n_jobs; i0 = next_chunk(i0, n_jobs)) {
+    std::memset(&P, 0, sizeof(P));
+    SeqPlan p;
+    const int st = plan_launch(jobs + i0, next_chunk(i0, n_jobs) - i0, batch, info, &P, &p);
+    if (st != Q4K_OK) return st;
+    if (p.n_epoch == 0) continue;
+    P.sync = reinterpret_cast<unsigned*>(ws);
+    P.tickets = reinterpret_cast<unsigned*>(ws + p.tickets_off);
+    P.pieces = reinterpret_cast<float*>(ws + p.pieces_off);
+    P.err = err;
+    cudaError_t e;
+    switch (batch) {
+      case 1: e = launch_seq_b<1>(P, p, dev, info, s); break;
+      case 2: e = launch_seq_b<2>(P, p, dev, info, s); break;
+      case 3: e = launch_seq_b<3>(P, p, dev, info, s); break;
+      case 4: e = launch_seq_b<4>(P, p, dev, info, s); break;
+      case 5: e = launch_seq_b<5>(P, p, dev, info, s); break;
+      case 6: e = launch_seq_b<6>(P, p, dev, info, s); break;
+      case 7: e = launch_seq_b<7>(P, p, dev, info, s); break;
+      case 8: e = launch_seq_b<8>(P, p, dev, info, s); break;
+      default: return Q4K_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) {
+      *cuda_err = e;
+      return Q4K_ERR_CUDA;
+    }
+  }
+  return Q4K_OK;
 }
 
 }  // namespace q4k

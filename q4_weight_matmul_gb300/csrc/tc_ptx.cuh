@@ -94,6 +94,18 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
   return ok != 0;
 }
 
+// Bounded wait without an abort flag and without a suspend-time hint: the
+// thread polls try_wait (which itself blocks only briefly), so it resumes as
+// soon as the phase completes.  For waits on the critical path of a stream.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kTimeoutCycles) return false;
+  }
+}
+
 // Bounded wait without an abort flag.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;

@@ -179,6 +179,30 @@ int q4k_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * q4k_gemv_seq_static - q4k_gemv_seq for callers that cannot allocate device
+ * memory: a serving process that fixes its device memory at start-up and may
+ * not allocate afterwards, a plug-in that runs inside a host program whose
+ * allocator it may not touch, or plain C code with no allocator at all.  The
+ * pages have no counterpart; it is an addition for such callers.
+ * Same jobs, batch, layout, results and accuracy as q4k_gemv_seq, but no
+ * workspace argument: the scratch is a fixed 1 MiB array in the library's
+ * device memory, which every GPU that loads the library holds until the
+ * process exits.  The call itself allocates nothing (no cudaMalloc, no
+ * allocating library routine).
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and keeps it; make that first call before any
+ *    stream capture.
+ *  - Each call first clears the array's counters on `stream`, then launches.
+ *  - All calls on a device share the one array: calls that overlap on the
+ *    GPU (other streams, other host threads) race and give wrong results.
+ *  - A job list whose scratch would exceed 1 MiB (the need grows with the
+ *    batch and the SM count; a GB300 at batch 8 needs about 0.6 MiB) gives
+ *    Q4K_ERR_UNSUPPORTED and enqueues nothing.
+ */
+int q4k_gemv_seq_static(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch,
+                        void* stream);
+
+/*
  * q4k_gemm - prefill MMQ GEMM (genie-ai-runtime §3, "The tensor-core kernel
  * (Path E)"; integer form over q8_1 activations):
  *   y[t][o] = sum_b ( d*sc[o,b] * d8[t,b] * P[t,o,b]

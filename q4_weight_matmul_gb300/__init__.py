@@ -43,6 +43,7 @@ SIGNATURES = {
     "q4k_gemv_multi": (_I, [_I, _P, _I, _P, _I64, _P, _I64, _P, _P, _P]),
     "q4k_gemv_seq_workspace_bytes": (ctypes.c_size_t, [_P, _I, _I64]),
     "q4k_gemv_seq": (_I, [_P, _I, _I, _I64, _P, ctypes.c_size_t, _P]),
+    "q4k_gemv_seq_static": (_I, [_P, _I, _I, _I64, _P]),
     "q4k_gemm": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
     "q4k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
     "q4k_device_error": (_I, [_P]),
@@ -215,6 +216,23 @@ def q4k_gemv_seq(jobs, batch: int, layout: int = BLOCK144, workspace=None, strea
     return seq
 
 
+def q4k_gemv_seq_static(jobs, batch: int, layout: int = BLOCK144, stream=None):
+    """``q4k_gemv_seq`` without a workspace: the library's built-in scratch
+    array serves instead, so nothing is allocated (for callers that cannot
+    allocate device memory).  Calls that overlap on the GPU race."""
+    n = len(jobs)
+    arr = (GemvJob * max(n, 1))()
+    for i, j in enumerate(jobs):
+        arr[i].w = _ptr(j["w"], torch.uint8, "w")
+        arr[i].rows = int(j["rows"])
+        arr[i].cols = int(j["cols"])
+        arr[i].x = _ptr(j["x"], torch.float32, "x")
+        arr[i].residual = _ptr(j.get("residual"), torch.float32, "residual")
+        arr[i].y = _ptr(j["y"], torch.float32, "y")
+        arr[i].wait = 1 if j.get("wait") else 0
+    _check(lib().q4k_gemv_seq_static(arr, n, layout, int(batch), _stream(stream)), "q4k_gemv_seq_static")
+
+
 def q4k_gemm(w, rows: int, cols: int, q8, d8, s, y=None, layout: int = BLOCK144, stream=None):
     """Prefill MMQ GEMM on q8_1 activations; returns ``y`` [tokens][rows] float32."""
     tokens = q8.shape[0]
@@ -255,7 +273,7 @@ def q4k_version() -> str:
 
 
 __all__ = ["build", "lib", "Q4KError", "BLOCK144", "q4k_packed_bytes", "q4k_pack", "q8_quantize",
-           "q4k_gemv", "q4k_gemv_multi", "GemvJob", "GemvSeq", "q4k_gemv_seq", "q4k_gemm",
+           "q4k_gemv", "q4k_gemv_multi", "GemvJob", "GemvSeq", "q4k_gemv_seq", "q4k_gemv_seq_static", "q4k_gemm",
            "q4k_gemm_blockdots", "q4k_device_error",
            "q4k_selftest_wait_timeout", "q4k_version",
            "SIGNATURES"]

@@ -268,6 +268,16 @@ int q4k_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch
   return st;
 }
 
+int q4k_gemv_seq_static(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch, void* stream) {
+  bool work = false;
+  if (int e = check_seq(jobs, n_jobs, layout, batch, &work)) return e;
+  if (!work) return Q4K_OK;
+  cudaError_t ce = cudaSuccess;
+  const int st = launch_gemv_seq_static(jobs, n_jobs, (int)batch, static_cast<cudaStream_t>(stream), &ce);
+  if (st == Q4K_ERR_CUDA) return record_cuda(ce);
+  return st;
+}
+
 int q4k_selftest_wait_timeout(void* stream) {
   int* err = device_error_word();
   if (!err) return record_cuda(cudaGetLastError());

@@ -49,6 +49,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 namespace q4k {
 namespace {
@@ -679,6 +680,52 @@ int launch_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int batch, void* works
     }
   }
   return Q4K_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Variant that allocates nothing: the workspace is a fixed array in this
+// library's device memory instead of caller-provided memory.
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;   // 1 MiB
+std::mutex g_static_mutex;
+void* g_static_ptr[64];
+}  // namespace
+
+// Built-in workspace of q4k_gemv_seq_static.  Every GPU that loads the
+// library holds it until the process exits; all calls on a device share it.
+static __device__ __align__(256) unsigned char g_seq_scratch[kStaticScratchBytes];
+
+int launch_gemv_seq_static(const q4k_gemv_job* jobs, int n_jobs, int batch, cudaStream_t s,
+                           cudaError_t* cuda_err) {
+  *cuda_err = cudaSuccess;
+  int dev = 0;
+  if ((*cuda_err = cudaGetDevice(&dev)) != cudaSuccess) return Q4K_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return Q4K_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    // host code only knows the array's device address once it asks for it,
+    // with the device current; the answer is kept per device
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!g_static_ptr[dev]) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_seq_scratch);
+      if (e != cudaSuccess) {
+        *cuda_err = e;
+        return Q4K_ERR_CUDA;
+      }
+      g_static_ptr[dev] = p;
+    }
+    scratch = g_static_ptr[dev];
+  }
+  size_t need = 0;
+  const int st = gemv_seq_workspace(jobs, n_jobs, batch, &need);
+  if (st != Q4K_OK) return st;
+  if (need > kStaticScratchBytes) return Q4K_ERR_UNSUPPORTED;
+  // the arrival counters and tickets must start at zero; a launch that runs
+  // to its end leaves them so, and this also covers one that never did
+  const size_t counters = kSyncBytes + (((sizeof(unsigned) * 2 * (size_t)device_info(dev).sm_count) + 255) & ~size_t(255));
+  if ((*cuda_err = cudaMemsetAsync(scratch, 0, counters, s)) != cudaSuccess) return Q4K_ERR_CUDA;
+  return launch_gemv_seq(jobs, n_jobs, batch, scratch, kStaticScratchBytes, s, cuda_err);
 }
 
 }  // namespace q4k

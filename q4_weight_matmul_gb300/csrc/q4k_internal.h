@@ -50,6 +50,9 @@ constexpr int kGemvSeqMaxJobs = 256;
 int gemv_seq_workspace(const q4k_gemv_job* jobs, int n_jobs, int batch, size_t* bytes);
 int launch_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int batch, void* workspace, size_t workspace_bytes,
                     cudaStream_t s, cudaError_t* cuda_err);
+// The same with the library's built-in scratch array as the workspace.
+int launch_gemv_seq_static(const q4k_gemv_job* jobs, int n_jobs, int batch, cudaStream_t s,
+                           cudaError_t* cuda_err);
 
 // Small-tile integer MMQ on CUDA cores (dp4a).  When `p_out` is non-null
 // the kernel stores the raw per-block integer dots there instead of y.

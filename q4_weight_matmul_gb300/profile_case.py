@@ -4,6 +4,11 @@
     python -m q4_weight_matmul_gb300.profile_case gemm --rows 9728 --cols 2560 --tokens 512
     python -m q4_weight_matmul_gb300.profile_case q8 --tokens 512 --cols 9728
     python -m q4_weight_matmul_gb300.profile_case pack --rows 9728 --cols 2560
+    python -m q4_weight_matmul_gb300.profile_case seq --layers 13 --batch 1 --reps 3
+
+``seq`` runs --layers Qwen3-4B-shaped decode linear sets (q, k, v, o, gate,
+up, down; independent inputs) as one q4k_gemv_seq launch per rep, as the
+benchmark does (13 sets per launch).
 
 Inputs are uniformly random bytes / N(0,1) floats (valid Q4_K fields), made on
 the device; nothing is checked here (the tests do that).  Weights are spread
@@ -29,9 +34,31 @@ def rand_fields(rows, cols, dev, gen):
     return d, dmin, sc, m, q
 
 
+QWEN3_4B_LAYER = (("q", 4096, 2560, 0), ("k", 1024, 2560, 0), ("v", 1024, 2560, 0), ("o", 2560, 4096, 1),
+                  ("gate", 9728, 2560, 2), ("up", 9728, 2560, 2), ("down", 2560, 9728, 3))
+
+
+def run_seq(a, dev, gen):
+    xs = [torch.randn((a.batch, c), device=dev, generator=gen) for c in (2560, 4096, 2560, 9728)]
+    jobs = []
+    for _ in range(a.layers):
+        for name, rows, cols, inp in QWEN3_4B_LAYER:
+            w = q4k.q4k_pack(*rand_fields(rows, cols, dev, gen))
+            jobs.append({"w": w, "rows": rows, "cols": cols, "x": xs[inp],
+                         "y": torch.empty((a.batch, rows), device=dev)})
+    seq = q4k.GemvSeq(jobs, a.batch)
+    for _ in range(a.reps):
+        seq()
+    torch.cuda.synchronize()
+    if q4k.q4k_device_error() != 0:
+        raise RuntimeError("a kernel gave up a bounded wait")
+    print("profile case done: seq", a.layers, "layers, batch", a.batch, a.reps, "reps")
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["gemv", "gemm", "q8", "pack"])
+    ap.add_argument("kernel", choices=["gemv", "gemm", "q8", "pack", "seq"])
+    ap.add_argument("--layers", type=int, default=13)
     ap.add_argument("--rows", type=int, default=9728)
     ap.add_argument("--cols", type=int, default=2560)
     ap.add_argument("--batch", type=int, default=1)
@@ -42,6 +69,9 @@ def main():
     dev = torch.device("cuda", 0)
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
+    if a.kernel == "seq":
+        run_seq(a, dev, gen)
+        return
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
     f = rand_fields(a.rows, a.cols, dev, gen)
     w0 = q4k.q4k_pack(*f)

@@ -6,7 +6,7 @@
 // One CTA per SM stays resident for the whole list.  Its producer thread
 // streams weights into a shared-memory ring with 3-D tensor copies and waits
 // for nothing but a free slot, so the weight stream runs on across matrix
-// boundaries and across the dependency points between jobs; 16 consumer
+// boundaries and across the dependency points between jobs; 15 consumer
 // warps dequantise and reduce.  This removes the launch gap, the start-up
 // latency and the drain that separate launches pay at every matrix boundary.
 //
@@ -54,7 +54,7 @@
 namespace q4k {
 namespace {
 
-constexpr int kConsumerWarps = 16;
+constexpr int kConsumerWarps = 15;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;          // + one producer warp
 constexpr int kRB = 32;                            // rows per block (one per lane)
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
         staged_nb = nb;
         named_sync_consumers();
       }
-      const int pu = P.part_floats / per;   // units per pass, a multiple of 16
+      const int pu = P.part_floats / per;   // units per pass
       for (int ps = 0; ps < n_units; ps += pu, ++pass_no) {
         const int pe = min(ps + pu, n_units);
         consume_pass<B>(P, ring_base, full, empty, issued, ring, J, ps, pe, u0, nb, nu, xs, xss, part, ok, warp,

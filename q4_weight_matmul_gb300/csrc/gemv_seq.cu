@@ -84,6 +84,7 @@ struct SeqEpoch {
   long long units;       // units of all its segments
   int seg_begin, seg_end;
   int ctas;              // CTAs sharing its units (<= grid)
+  int aligned;           // CTA ranges start on row-block boundaries (no shared row blocks)
 };
 
 struct SeqParams {
@@ -157,12 +158,26 @@ __device__ __noinline__ bool grid_wait(const unsigned* counter, unsigned target)
   return true;
 }
 
-// First unit of CTA c's range in epoch E (c = ctas gives the end).
-__device__ __forceinline__ long long range_begin(const SeqEpoch& E, int c) {
-  return (long long)c * E.units / E.ctas;
+// The segment of epoch E that holds epoch unit u.
+__device__ __forceinline__ int seg_of(const SeqParams& P, const SeqEpoch& E, long long u) {
+  int s = E.seg_begin;
+  while (s + 1 < E.seg_end && u >= P.seg[s + 1].unit_base) ++s;
+  return s;
 }
 
-// The CTA whose range holds epoch unit u.
+// First unit of CTA c's range in epoch E (c = ctas gives the end): an equal
+// share, or, in an aligned epoch, that share moved back to the start of its
+// row block (then no row block is shared and nothing has to be combined;
+// some CTAs may get no units).
+__device__ __forceinline__ long long range_begin(const SeqParams& P, const SeqEpoch& E, int c) {
+  const long long u = (long long)c * E.units / E.ctas;
+  if (!E.aligned || c >= E.ctas) return u;
+  const SeqSeg& S = P.seg[seg_of(P, E, u)];
+  return S.unit_base + (u - S.unit_base) / S.nu * S.nu;
+}
+
+// The CTA whose range holds epoch unit u (in epochs that are not aligned;
+// only those share row blocks).
 __device__ __forceinline__ int owner_of(const SeqEpoch& E, long long u) {
   return (int)(((u + 1) * E.ctas + E.units - 1) / E.units - 1);
 }
@@ -177,7 +192,7 @@ __device__ __forceinline__ int job_of(const SeqParams& P, const SeqSeg& S, long 
 // [f, f + nu): side 0 if it is c's first row block, else side 1.
 __device__ __forceinline__ float* piece_of(const SeqParams& P, const SeqEpoch& E, int slot, int grid, int c,
                                            long long f, int nu, int B) {
-  const long long u0 = range_begin(E, c);
+  const long long u0 = (long long)c * E.units / E.ctas;
   const int side = (u0 >= f && u0 < f + nu) ? 0 : 1;
   return P.pieces + (((size_t)slot * grid + c) * 2 + side) * (size_t)(kRB * B);
 }
@@ -262,13 +277,6 @@ __device__ __forceinline__ void reduce_pass(const SeqParams& P, const SeqSeg& S,
   }
 }
 
-// The segment of epoch E that holds epoch unit u.
-__device__ __forceinline__ int seg_of(const SeqParams& P, const SeqEpoch& E, long long u) {
-  int s = E.seg_begin;
-  while (s + 1 < E.seg_end && u >= P.seg[s + 1].unit_base) ++s;
-  return s;
-}
-
 template <int B>
 __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_constant__ SeqParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -307,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
       for (int ei = 0; ei < P.n_epoch && pok; ++ei) {
         const SeqEpoch& E = P.epoch[ei];
         if (c >= E.ctas) continue;
-        const long long e1 = range_begin(E, c + 1);
-        long long u = range_begin(E, c);
+        const long long e1 = range_begin(P, E, c + 1);
+        long long u = range_begin(P, E, c);
         int si = seg_of(P, E, u);
         while (u < e1 && pok) {
           const SeqSeg& S = P.seg[si];
@@ -362,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
     const int slot = ei & 1;
     long long e0 = 0, e1 = 0;
     if (c < E.ctas) {
-      e0 = range_begin(E, c);
-      e1 = range_begin(E, c + 1);
+      e0 = range_begin(P, E, c);
+      e1 = range_begin(P, E, c + 1);
     }
     if (ei > 0) {
       // activations may be outputs of earlier jobs: wait for all of them
@@ -474,6 +482,38 @@ struct SeqPlan {
   size_t smem, ws_bytes, tickets_off, pieces_off;
 };
 
+// Whether an epoch's CTA ranges should start on row-block boundaries.  The
+// equal shares cost the largest share plus, when a boundary falls inside a
+// row block, the combine of shared row blocks at the epoch's end (a ticket
+// and a gather through L2: measured at 2-3 us, about kCombineUnits units of
+// streaming); the aligned ranges cost their largest range.  The smaller
+// estimate wins: small epochs (a decode layer's o or down projection in
+// engine order) go aligned, large ones keep equal shares.
+constexpr long long kCombineUnits = 12;
+
+bool choose_aligned(const SeqEpoch& E, const SeqSeg* seg) {
+  auto seg_at = [&](long long u) {
+    int s = E.seg_begin;
+    while (s + 1 < E.seg_end && u >= seg[s + 1].unit_base) ++s;
+    return s;
+  };
+  auto snapped = [&](int c) -> long long {
+    const long long u = (long long)c * E.units / E.ctas;
+    if (c >= E.ctas) return u;
+    const SeqSeg& S = seg[seg_at(u)];
+    return S.unit_base + (u - S.unit_base) / S.nu * S.nu;
+  };
+  long long equal_max = 0, aligned_max = 0;
+  bool shared = false;
+  for (int c = 0; c < E.ctas; ++c) {
+    const long long u0 = (long long)c * E.units / E.ctas, u1 = (long long)(c + 1) * E.units / E.ctas;
+    equal_max = std::max(equal_max, u1 - u0);
+    if (c > 0 && snapped(c) != u0) shared = true;
+    aligned_max = std::max(aligned_max, snapped(c + 1) - snapped(c));
+  }
+  return aligned_max < equal_max + (shared ? kCombineUnits : 0);
+}
+
 // Segments, epochs, row blocks and CTA shares of one launch's jobs (at most
 // kLaunchJobs).  Fills P (if not null) and the plan; returns a status.
 int plan_launch(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& info, SeqParams* P,
@@ -543,6 +583,7 @@ int plan_launch(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& i
     if (units / p.grid > (int64_t(1) << 30)) return Q4K_ERR_UNSUPPORTED;
     E.units = units;
     E.ctas = (int)std::min<int64_t>(p.grid, units);
+    E.aligned = choose_aligned(E, tseg) ? 1 : 0;
   }
   // shared memory: activations, partial sums, then the deepest ring that fits
   p.part_floats = 16 * kRB * B * (B <= 2 ? 8 : (B <= 4 ? 2 : 1));

@@ -7,7 +7,7 @@
 // Work split.  Rows are cut into blocks of RB rows (RB = 32, 16 or 8, chosen
 // so that the busiest SM holds the fewest rows); one CTA per SM owns a run of
 // row blocks (of one or several matrices) and all their superblocks.  A unit
-// of work is one row block x one superblock; the 16 consumer warps take units
+// of work is one row block x one superblock; the 15 consumer warps take units
 // round-robin, so K is split across warps.  Each unit leaves one partial sum
 // per row in shared memory and the CTA adds a row's partials in superblock
 // order (bitwise deterministic).
@@ -15,11 +15,12 @@
 // Streaming.  A producer warp fetches the weights with 3-D tensor copies:
 // one copy per stage of RB rows x (128/RB) superblocks (18 KB, out-of-range
 // rows and superblocks zero-filled) into a ring of stages.  The copies start
-// at launch, before the activations are read.  A CTA stays under half of an
-// SM (<= 56 registers per thread, <= ~110 KB of shared memory) so that, when
-// launched as a programmatic dependent (opt-in, see pdl_mode), the next
-// GEMV's CTA can sit beside it; griddepcontrol.wait orders every activation
-// read after the previous kernel has completed.
+// at launch, before the activations are read.  The CTA keeps its shared
+// memory under ~110 KB when it can; with 16 warps it may use 128 registers
+// per thread, so when launched as a programmatic dependent (opt-in, see
+// pdl_mode) the next GEMV's CTA starts on an SM once this one has left it;
+// griddepcontrol.wait orders every activation read after the previous kernel
+// has completed.
 //
 // Lanes.  32/RB lanes share a row: with RB = 32 a lane owns a row's whole
 // superblock (256 weights), with RB = 16 half of it, with RB = 8 one 64-weight
@@ -43,7 +44,7 @@
 namespace q4k {
 namespace {
 
-constexpr int kConsumerWarps = 16;
+constexpr int kConsumerWarps = 15;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;     // + one producer warp
 constexpr int kStageSuper = 128;              // superblock-rows per stage (RB * SB)
@@ -96,7 +97,7 @@ __device__ __forceinline__ int mat_of(const GemvParams& P, int g) {
 
 // LPR: lanes per row (1, 2 or 4); RB = 32 / LPR rows per block.
 template <int B, int LPR>
-__global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1)) gemv_block144_kernel(
+__global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
     const __grid_constant__ GemvParams P) {
   constexpr int RB = 32 / LPR;              // rows per block
   constexpr int SB = kStageSuper / RB;      // superblocks per stage

@@ -158,11 +158,17 @@ __device__ __noinline__ bool grid_wait(const unsigned* counter, unsigned target)
   return true;
 }
 
-// The segment of epoch E that holds epoch unit u.
+// The segment of epoch E that holds epoch unit u (binary search: a CTA far
+// into a long epoch would otherwise walk dozens of segments, each a load
+// from the kernel's parameter space, before its first copy).
 __device__ __forceinline__ int seg_of(const SeqParams& P, const SeqEpoch& E, long long u) {
-  int s = E.seg_begin;
-  while (s + 1 < E.seg_end && u >= P.seg[s + 1].unit_base) ++s;
-  return s;
+  int lo = E.seg_begin, hi = E.seg_end - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.seg[mid].unit_base <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
 // First unit of CTA c's range in epoch E (c = ctas gives the end): an equal
@@ -182,10 +188,15 @@ __device__ __forceinline__ int owner_of(const SeqEpoch& E, long long u) {
   return (int)(((u + 1) * E.ctas + E.units - 1) / E.units - 1);
 }
 
+// The job of segment S that holds row block rb (binary search).
 __device__ __forceinline__ int job_of(const SeqParams& P, const SeqSeg& S, long long rb) {
-  int j = S.job_begin;
-  while (j + 1 < S.job_end && rb >= P.job[j + 1].rb_base) ++j;
-  return j;
+  int lo = S.job_begin, hi = S.job_end - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.job[mid].rb_base <= rb) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
 // Piece held by CTA c of the row block whose units are epoch units
@@ -586,7 +597,7 @@ int plan_launch(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& i
     E.aligned = choose_aligned(E, tseg) ? 1 : 0;
   }
   // shared memory: activations, partial sums, then the deepest ring that fits
-  p.part_floats = 16 * kRB * B * (B <= 2 ? 8 : (B <= 4 ? 2 : 1));
+  p.part_floats = 16 * kRB * B * (B == 1 ? 16 : (B == 2 ? 8 : (B <= 4 ? 2 : 1)));
   p.ring = 0;
   for (int ring = kMaxRing; ring >= 4; --ring) {
     const size_t total = seq_layout(B, p.nb_max, p.part_floats, ring).total;

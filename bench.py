@@ -66,16 +66,26 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
 
 
+def code_digest(path: str) -> str:
+    """First 16 hex digits of the SHA-256 of a C/C++/CUDA source with its
+    comments and all white space removed: it changes when the code does,
+    not when a comment does."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    text = re.sub(r"\s+", "", text)
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def profile_traffic(kernel_tag: str, source: str):
     """DRAM bytes per launch recorded from an ncu capture in profiles/, valid
-    only while the kernel's source file is unchanged since the capture."""
+    only while the kernel's code is unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}_traffic.txt")
     try:
         text = open(path).read()
     except OSError:
         return None
-    src = open(os.path.join(ROOT, "q4_weight_matmul_gb300", "csrc", source), "rb").read()
-    digest = hashlib.sha256(src).hexdigest()[:16]
+    digest = code_digest(os.path.join(ROOT, "q4_weight_matmul_gb300", "csrc", source))
     m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     if not m_hash or not m_bytes or m_hash.group(1) != digest:

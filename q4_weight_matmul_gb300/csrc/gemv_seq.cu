@@ -24,14 +24,19 @@
 // row r without bank conflicts and all 32 lanes read the same activations
 // (broadcast).  On GB300 a tensor copy costs the copy engine a roughly fixed
 // time: boxes of 4.6 KB stream at about half the HBM rate, boxes of 9 KB and
-// more at nearly all of it.  An
-// epoch's units (its segments in order, each row-block-major) are cut into
-// equal contiguous ranges, one per CTA, so every SM streams the same number
-// of bytes whatever the matrix shapes, and a CTA stages new activations only
-// where its range enters another segment.  A row block cut by range
-// boundaries is finished by several CTAs: each stores its partial row sums in
-// the workspace and the last one to finish adds the pieces in CTA order (the
-// result does not depend on timing) and stores y.
+// more at nearly all of it.
+//
+// Work split.  An epoch's units (its segments in order, each
+// row-block-major) are cut into equal contiguous ranges, one per CTA, so
+// every SM streams the same number of bytes whatever the matrix shapes, and
+// a CTA stages new activations only where its range enters another segment.
+// A row block cut by range boundaries is finished by several CTAs: each
+// stores its partial row sums in the workspace and the last one to finish
+// adds the pieces in CTA order (the result does not depend on timing) and
+// stores y.  For a small epoch, where that final combine would cost more
+// than the imbalance, the range boundaries move back to row-block starts
+// instead (choose_aligned).  A launch takes up to 96 jobs (their tensor maps
+// travel in the kernel parameters); longer lists take several launches.
 //
 // Reduction.  Consumer warps take the CTA's units round-robin; each unit
 // leaves one partial per row in shared memory, and after a pass of units the

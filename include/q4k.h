@@ -148,10 +148,11 @@ size_t q4k_gemv_seq_workspace_bytes(const q4k_gemv_job* jobs, int n_jobs, int64_
 
 /*
  * q4k_gemv_seq - an ordered list of decode GEMVs in ONE persistent launch
- * (genie-ai-runtime §4, Path C: the GEMVs are the hot decode kernels, and
- * every decode step streams the whole model's weights; §2: decode is bound
- * by memory bandwidth).  One CTA per SM streams the weights of job after job
- * without a launch boundary; a job with `wait` set reads its activations
+ * per 96 jobs (genie-ai-runtime §4, Path C: the GEMVs are the hot decode
+ * kernels, and every decode step streams the whole model's weights; §2:
+ * decode is bound by memory bandwidth).  One CTA per SM streams the weights
+ * of job after job without a launch boundary, each SM the same share of the
+ * bytes between two `wait` points; a job with `wait` set reads its activations
  * only after every earlier job has completed, so it may consume an earlier
  * job's y (a decode layer: QKV | o | gate,up | down, each waiting on the
  * previous).  Jobs between two `wait` points may run concurrently: none of
@@ -162,10 +163,11 @@ size_t q4k_gemv_seq_workspace_bytes(const q4k_gemv_job* jobs, int n_jobs, int64_
  *   workspace : device memory of at least q4k_gemv_seq_workspace_bytes()
  *               bytes, 16-byte aligned, zero-filled before its first use
  *               (e.g. cudaMemset).  It holds the launch's arrival
- *               counters, which each call resets before it ends (also when
- *               its kernel gave up a bounded wait), so the workspace is
- *               reused without clearing.  Calls that share a workspace must
- *               not overlap on the GPU.
+ *               counters and tickets, which each call resets before it ends
+ *               (also when its kernel gave up a bounded wait), and the
+ *               partial row sums of row blocks that CTAs share, which need
+ *               no clearing; the workspace is reused as it is.  Calls that
+ *               share a workspace must not overlap on the GPU.
  * The launch is cooperative (every CTA resident at once, one per SM); it
  * fails with Q4K_ERR_CUDA when the GPU cannot hold them all.
  * Accuracy as q4k_gemv: |y - exact| <= 1e-4 * sum_k |w||x| (+|residual|).

@@ -26,7 +26,12 @@ Readings where the pages are silent (each is listed in the design notes):
 * q8_1: ``d8 = amax/127`` (fp32 division), ``q = round(x/d8)`` with fp32
   division and ties away from zero, clamped to [-127, 127]; a block whose
   ``d8`` is zero quantises to all zeros;
-* tolerance of the fp outputs: ``|y - y_ref| <= 1e-4 * sum_k |w||x|``.
+* tolerance of the fp outputs: ``|y - y_ref| <= 1e-4 * sum_k |w||x|``; a
+  kernel that applies a weight's scale term ``d*sc*q`` and its min term
+  ``dmin*m`` as separate sums (the MMQ form does by definition) is also held
+  to the bound with the magnitude normaliser
+  ``sum_k (|d*sc*q| + |dmin*m|) |x|`` (``magnitude_norm``), which differs
+  from ``sum |w||x|`` only where the two terms of a weight cancel.
 
 Parity pins: every function here is pinned in ``tests/test_oracle_*.py``
 against hand-worked values, closed forms, invariants or brute force.
@@ -149,6 +154,35 @@ def gemv(fields: dict, x: np.ndarray, residual: np.ndarray | None = None):
         y = y + r
         norm = norm + np.abs(r)
     return y, norm
+
+
+def weight_terms(fields: dict):
+    """The two terms of every weight, ``a = (d*sc)*q`` and ``b = dmin*m``,
+    each evaluated with the same fp32 operations as ``dequantize`` (so that
+    ``w = a - b`` there)."""
+    q = np.asarray(fields["q"], np.uint8)
+    rows, cols = q.shape
+    d = f16_bits_to_f64(fields["d"]).astype(np.float32)
+    dmin = f16_bits_to_f64(fields["dmin"]).astype(np.float32)
+    d_k = np.repeat(d.reshape(rows, -1), QK_K, axis=1)
+    dmin_k = np.repeat(dmin.reshape(rows, -1), QK_K, axis=1)
+    sc_k = np.repeat(np.asarray(fields["sc"]).reshape(rows, -1), QK_SUB, axis=1).astype(np.float32)
+    m_k = np.repeat(np.asarray(fields["m"]).reshape(rows, -1), QK_SUB, axis=1).astype(np.float32)
+    return (d_k * sc_k) * q.astype(np.float32), dmin_k * m_k
+
+
+def magnitude_norm(fields: dict, x: np.ndarray, residual: np.ndarray | None = None):
+    """``sum_k (|a_k| + |b_k|) |x_k|`` (+ ``|residual|``) in float64,
+    ``[batch][rows]``, with ``a``, ``b`` the two terms of each weight
+    (``weight_terms``); for the MMQ path ``x`` is ``dequantize_q8_1(q8, d8)``.  It is at least ``sum_k |w_k||x_k|`` (up to the fp32
+    rounding of ``a - b``) and equal to it wherever ``b = 0``."""
+    a, b = weight_terms(fields)
+    mag = np.abs(a).astype(np.float64) + np.abs(b).astype(np.float64)
+    x64 = np.atleast_2d(np.asarray(x)).astype(np.float64)    # float32 x, or the float64 d8*q8
+    norm = np.abs(x64) @ mag.T
+    if residual is not None:
+        norm = norm + np.abs(np.atleast_2d(np.asarray(residual, np.float32)).astype(np.float64))
+    return norm
 
 
 # --------------------------------------------------------------------------

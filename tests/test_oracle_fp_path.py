@@ -115,3 +115,35 @@ def test_tolerance_helper_rejects_a_planted_error():
     bad[0, 2] += 2e-4 * norm[0, 2]
     ok, worst = O.within_tolerance(bad, y, norm)
     assert not ok and worst > 1.5
+
+
+def test_magnitude_norm_hand_worked_cancellation():
+    # one superblock, d = 1, dmin = 1; sub-block 0 has sc = 2, m = 6 and
+    # q = 3 everywhere, so every weight is 2*3 - 1*6 = 0 (sum |w||x| = 0)
+    # while each term has magnitude 6; the other sub-blocks have m = 0
+    f = {"d": np.array([[0x3C00]], np.uint16), "dmin": np.array([[0x3C00]], np.uint16),
+         "sc": np.array([[2, 1, 1, 1, 1, 1, 1, 1]], np.uint8),
+         "m": np.array([[6, 0, 0, 0, 0, 0, 0, 0]], np.uint8),
+         "q": np.full((1, 256), 3, np.uint8)}
+    x = np.ones((1, 256), np.float32)
+    x[0, :32] = np.arange(32, dtype=np.float32) - 10.5
+    y, norm = O.gemv(f, x)
+    mag = O.magnitude_norm(f, x)
+    s0 = float(np.abs(x[0, :32]).astype(np.float64).sum())
+    # sub-block 0: w = 0, |a| + |b| = 12; sub-blocks 1..7: w = a = 3, b = 0
+    assert norm[0, 0] == 3.0 * 224
+    assert mag[0, 0] == 12.0 * s0 + 3.0 * 224
+    assert y[0, 0] == 3.0 * 224
+
+
+def test_magnitude_norm_equals_norm_without_mins_and_bounds_it():
+    f = synth.q4k_fields(7, 768, 91)
+    x = synth.activations(3, 768, 92)
+    mag = O.magnitude_norm(f, x)
+    _, norm = O.gemv(f, x)
+    assert np.all(norm <= mag * (1 + 2.0 ** -22))
+    f0 = dict(f, m=np.zeros_like(f["m"]))
+    _, norm0 = O.gemv(f0, x)
+    assert np.array_equal(O.magnitude_norm(f0, x), norm0)
+    r = synth.residual(3, 7, 93)
+    assert np.allclose(O.magnitude_norm(f, x, r) - mag, np.abs(r.astype(np.float64)), rtol=0, atol=1e-12)

@@ -1,4 +1,6 @@
 """Pins of the oracle's q8_1 quantisation and MMQ path (CPU only)."""
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
@@ -127,3 +129,38 @@ def test_mmq_single_superblock_closed_form():
     q8, d8, s = O.quantize_q8_1(np.full((1, 256), 127, np.float32))
     y, _ = O.mmq(f, q8, d8, s)
     assert y[0, 0] == 127 * 8384
+
+
+def _nearest_f32(v: Fraction) -> np.float32:
+    """The float32 nearest to the rational v (ties to even), by exact search."""
+    c = np.float32(float(v))
+    best = c
+    for cand in (np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))):
+        dc, db = abs(Fraction(float(cand)) - v), abs(Fraction(float(best)) - v)
+        if dc < db or (dc == db and (int(cand.view(np.uint32)) & 1) == 0):
+            best = cand
+    return best
+
+
+def test_scale_divides_rather_than_multiplying_by_a_reciprocal():
+    # amax = 932.5: d8 is the float32 nearest to 932.5/127.  x1 = 1.5*d8 and
+    # x3 = 0.5*d8 are exact float32 values, so x/d8 is exactly 1.5 and 0.5
+    # and rounds away from zero to 2 and 1.  Multiplying by the float32
+    # reciprocal of d8 instead gives 1.4999999 and 0.49999997 (q = 1 and 0):
+    # this block tells the two readings apart.
+    d8_exact = _nearest_f32(Fraction(9325, 10) / 127)
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0] = 932.5
+    x[0, 1] = np.float32(float(Fraction(3, 2) * Fraction(float(d8_exact))))
+    x[0, 2] = -x[0, 1]
+    x[0, 3] = np.float32(float(Fraction(1, 2) * Fraction(float(d8_exact))))
+    assert Fraction(float(x[0, 1])) == Fraction(3, 2) * Fraction(float(d8_exact))
+    assert Fraction(float(x[0, 3])) == Fraction(1, 2) * Fraction(float(d8_exact))
+    q, d8, s = O.quantize_q8_1(x)
+    assert d8[0, 0] == d8_exact
+    assert list(q[0, :4]) == [127, 2, -2, 1]
+    assert s[0, 0] == 127 + 2 - 2 + 1
+    # the reciprocal reading differs on exactly these elements
+    recip = np.float32(1.0) / d8_exact
+    assert np.float32(x[0, 1] * recip) < np.float32(1.5)
+    assert np.float32(x[0, 3] * recip) < np.float32(0.5)

@@ -5,13 +5,19 @@ Headline: decode GEMV HBM GB/s at batch 1 over the Qwen3-4B-shaped decode
 linear set (q 4096x2560, k/v 1024x2560, o 2560x4096, gate/up 9728x2560,
 down 2560x9728; synthetic Q4_K weights, independent N(0,1) activations).  One
 step runs the seven GEMVs of one set; consecutive steps read different
-copies of the layer so that no step finds its weights in L2, and 13 steps
-share one persistent q4k_gemv_seq launch.  Beside it: the same layer in
-engine order (each group waits for the previous one), and the 36-layer stack
-per decode token at batch 1 and 4.
+copies of the layer so that no step finds its weights in L2, and the steps
+are split evenly over persistent q4k_gemv_seq launches of at most 13 sets.
+The timed unit is one CUDA-graph replay of exactly `steps` steps; the graph
+is replayed back to back for about a second while nvidia-smi samples the
+clocks, and the value comes from the median replay.
 
-Second leg (same JSON line, key "prefill"): q8_1 quantisation plus the MMQ
-GEMM of the 512-token Qwen3-4B prefill (gate 9728x2560, down 2560x9728).
+Beside it (same JSON line): the decode layer and the 36-layer decode token
+in engine order (each input group waits for the previous group's output),
+the 36-layer stack as independent jobs, batch 4, the single 2048x2048 GEMV
+(L2-resident latency), the public API end to end with host buffers, and
+the prefill GEMMs: 512 tokens (gate + down), the 2048-token 36-layer stack,
+the 4096-token Qwen3-8B MLP, and 8..64-token short prompts.  The oracle is
+timed on the host cores (one core and all cores) as the CPU baseline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -44,11 +50,13 @@ import synth  # noqa: E402
 METRIC = "Q4_K GEMV HBM GB/s (batch 1, % of peak); prefill GEMM int8 TOPS & tok/s"
 WORKLOAD = ("Qwen3-4B-shaped decode linear set, batch 1: q 4096x2560, k/v 1024x2560, "
             "o 2560x4096, gate/up 9728x2560, down 2560x9728 (Q4_K)")
-PREFILL_WORKLOAD = "512-token prefill: q8_1 X[512x2560] x gate 9728x2560, X_down[512x9728] x down 2560x9728"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_HBM_GBS = 8000.0
 BYTES_PER_WEIGHT = 144.0 / 256.0
-STEPS_PER_LAUNCH = 13          # 91 GEMV jobs per q4k_gemv_seq launch (at most 96)
+MAX_SETS_PER_LAUNCH = 13       # 91 GEMV jobs per q4k_gemv_seq launch (at most 96)
+REPLAY_SECONDS = 1.0           # back-to-back replays of each headline graph
+MIN_REPLAYS = 20
 
 
 def log(*a):
@@ -77,7 +85,13 @@ def code_digest(path: str) -> str:
     return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
-def profile_traffic(kernel_tag: str, source: str):
+def kernel_digest(sources) -> str:
+    """Digest over several sources (a kernel and the headers it includes)."""
+    csrc = os.path.join(ROOT, "q4_weight_matmul_gb300", "csrc")
+    return hashlib.sha256("".join(code_digest(os.path.join(csrc, s)) for s in sources).encode()).hexdigest()[:16]
+
+
+def profile_traffic(kernel_tag: str, source):
     """DRAM bytes per launch recorded from an ncu capture in profiles/, valid
     only while the kernel's code is unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}_traffic.txt")
@@ -85,7 +99,9 @@ def profile_traffic(kernel_tag: str, source: str):
         text = open(path).read()
     except OSError:
         return None
-    digest = code_digest(os.path.join(ROOT, "q4_weight_matmul_gb300", "csrc", source))
+    sources = [source] if isinstance(source, str) else list(source)
+    digest = code_digest(os.path.join(ROOT, "q4_weight_matmul_gb300", "csrc", sources[0])) \
+        if len(sources) == 1 else kernel_digest(sources)
     m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     if not m_hash or not m_bytes or m_hash.group(1) != digest:
@@ -112,6 +128,15 @@ def job_throughput(bytes_per_step: float, steps: int, world: int, max_ms: float)
     return bytes_per_step * steps * world / (max_ms * 1e-3) / 1e9
 
 
+def even_split(count: int, max_per: int) -> list[int]:
+    """``count`` items in the fewest groups of at most ``max_per``, sizes
+    differing by at most one (no short tail group)."""
+    if count <= 0:
+        return []
+    n = -(-count // max_per)
+    return [count // n + (1 if i < count % n else 0) for i in range(n)]
+
+
 # --------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
@@ -124,6 +149,7 @@ class ClockSampler:
         self.rows = []
         self.proc = None
         self.thread = None
+        self.t_on = self.t_off = None
 
     def start(self):
         try:
@@ -140,19 +166,28 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) == 9:
-                self.rows.append(parts)
+                self.rows.append((time.perf_counter(), parts))
+
+    def mark(self, on: bool):
+        """Bracket the timed region: only samples inside it are kept."""
+        if on:
+            self.t_on = time.perf_counter()
+        else:
+            self.t_off = time.perf_counter()
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.15)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=5)
-        rows = self.rows
+        rows = [r for t, r in self.rows
+                if (self.t_on is None or t >= self.t_on) and (self.t_off is None or t <= self.t_off + 0.1)]
+        rows = rows or [r for _, r in self.rows]
         if self.uuid:
             mine = [r for r in rows if self.uuid in r[0] or r[0] in self.uuid]
             rows = mine or rows
@@ -180,16 +215,15 @@ def decode_inputs():
     return _DECODE_CACHE["layer"]
 
 
-def oracle_decode_sample(budget_s: float, seed_rows: int = 0):
+def oracle_decode_sample(budget_s: float, seed_rows: int = 0, per: int = 64):
     """Time the oracle GEMV on row samples of the seven decode matrices until
-    ``budget_s`` of CPU time is spent.  Returns (GB/s, seconds, description)."""
+    ``budget_s`` of wall time is spent.  Returns (GB/s, seconds, description)."""
     from oracle import q4k as O
     fields, xs = decode_inputs()
     rng = np.random.default_rng(seed_rows)
     done_bytes = 0.0
     spent = 0.0
     passes = 0
-    per = 64
     while spent < budget_s:
         for name, rows, cols, inp in synth.QWEN3_4B_LAYER:
             sel = np.sort(rng.choice(rows, per, replace=False))
@@ -203,27 +237,67 @@ def oracle_decode_sample(budget_s: float, seed_rows: int = 0):
     return done_bytes / spent / 1e9, spent, desc
 
 
+def oracle_gemm_sample(budget_s: float, rows_per: int = 48):
+    """Time the oracle MMQ (q8_1 quantisation + block dots + scales) on row
+    samples of the 512-token prefill (gate 9728x2560 and down 2560x9728, all
+    512 tokens).  Returns (integer TOPS, tok/s over the full problem, seconds,
+    description)."""
+    from oracle import q4k as O
+    pf, pxs = synth.prefill_4b_512()
+    rng = np.random.default_rng(7)
+    shapes = (("gate", 9728, 2560, "mlp_in"), ("down", 2560, 9728, "down_in"))
+    quant = {inp: O.quantize_q8_1(pxs[inp]) for _, _, _, inp in shapes}
+    spent, ops, rows_done, passes = 0.0, 0.0, 0, 0
+    while spent < budget_s:
+        for name, rows, cols, inp in shapes:
+            sel = np.sort(rng.choice(rows, rows_per, replace=False))
+            f = {k: v[sel] for k, v in pf[name].items()}
+            q, d8, s = quant[inp]
+            t0 = time.perf_counter()
+            O.mmq(f, q, d8, s)
+            spent += time.perf_counter() - t0
+            ops += 2.0 * 512 * rows_per * cols
+        passes += 1
+    full_ops = 2.0 * 512 * (9728 * 2560 + 2560 * 9728)
+    tops = ops / spent / 1e12
+    desc = (f"oracle MMQ on {passes} passes of {rows_per} random rows of gate and of down, all 512 tokens "
+            f"(q8_1 of the inputs computed once, outside the timing)")
+    return tops, 512 * tops * 1e12 / full_ops, spent, desc
+
+
 def cpu_threads() -> int:
     try:
-        import threadpoolctl  # noqa: F401
-        from threadpoolctl import threadpool_info
-        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
-        return int(n)
-    except Exception:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
         return os.cpu_count() or 1
+
+
+def single_core_decode(budget_s: float):
+    """The oracle GEMV sample in a child process pinned to one core with one
+    BLAS thread (a fresh interpreter, so the limits apply from its start)."""
+    code = ("import json,os,sys; sys.path.insert(0, %r); os.sched_setaffinity(0, {min(os.sched_getaffinity(0))});"
+            "import bench; g,s,d = bench.oracle_decode_sample(%r); print(json.dumps([g,s,d]))" % (ROOT, budget_s))
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                           timeout=budget_s * 10 + 120)
+        g, s, d = json.loads(r.stdout.strip().splitlines()[-1])
+        return {"value": g, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": d, "seconds": round(s, 2)}
+    except Exception as e:  # noqa: BLE001 - the baseline is reported, never required
+        return {"value": None, "error": f"{type(e).__name__}: {e}"[:200]}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
     # each step: a bounded oracle sample of the decode set (~1 s)
-    vals = []
     total_bytes = 0.0
     total_s = 0.0
+    desc = ""
     for i in range(args.warmup + args.steps):
         gbs, spent, desc = oracle_decode_sample(1.0, seed_rows=i)
         if i >= args.warmup:
-            vals.append(gbs)
             total_bytes += gbs * spent
             total_s += spent
     value = total_bytes / total_s
@@ -264,28 +338,50 @@ def run_ours(args, rank, world):
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
     uuid = str(getattr(props, "uuid", "") or "") or None
     peaks, peak_kind = measured_peaks()
-    stream = torch.cuda.current_stream()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    def time_graph(g, reps=5):
+        """Median over `reps` back-to-back replays (one warm replay first)."""
+        g.replay()
+        barrier()
+        evs = [(ev(), ev()) for _ in range(reps)]
+        for a, b in evs:
+            a.record()
+            g.replay()
+            b.record()
+        barrier()
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
 
     # ---------------- weights: pack once, then rotate copies to defeat L2
     fields, xs_np = decode_inputs()
     t_pack0 = time.perf_counter()
     packed = {}
     pack_bytes = 0
-    pack_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     dev_fields = {}
     for name, rows, cols, _ in synth.QWEN3_4B_LAYER:
         f = fields[name]
         dev_fields[name] = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev)
                             for k, v in f.items()}
     torch.cuda.synchronize()
-    pack_ev[0].record()
+    p0, p1 = ev(), ev()
+    p0.record()
     for name, rows, cols, _ in synth.QWEN3_4B_LAYER:
         d = dev_fields[name]
         packed[name] = q4k.q4k_pack(d["d"], d["dmin"], d["sc"], d["m"], d["q"])
         pack_bytes += sum(t.numel() * t.element_size() for t in d.values()) + packed[name].numel()
-    pack_ev[1].record()
+    p1.record()
     torch.cuda.synchronize()
-    pack_ms = pack_ev[0].elapsed_time(pack_ev[1])
+    pack_ms = p0.elapsed_time(p1)
     del dev_fields
     layer_bytes = sum(p.numel() for p in packed.values())
     n_copies = max(2, math.ceil(4 * l2 / layer_bytes))
@@ -296,91 +392,80 @@ def run_ours(args, rank, world):
     log(f"[bench] rank {rank}: {n_copies} layer copies x {layer_bytes / 1e6:.1f} MB, pack {pack_ms:.2f} ms "
         f"(setup {time.perf_counter() - t_pack0:.1f}s)")
 
-    step_bytes = 0.0
-    for name, rows, cols, _ in synth.QWEN3_4B_LAYER:
-        step_bytes += rows * cols * BYTES_PER_WEIGHT + cols * 4 + rows * 4
+    def set_bytes(batch):
+        return sum(rows * cols * BYTES_PER_WEIGHT + batch * (cols + rows) * 4
+                   for _, rows, cols, _ in synth.QWEN3_4B_LAYER)
 
+    step_bytes = set_bytes(1)
     shape = {name: (rows, cols, inp) for name, rows, cols, inp in synth.QWEN3_4B_LAYER}
-    # engine order: one launch per input group (QKV triple, o, gate/up pair, down)
+    # engine order: one group per input (QKV triple, o, gate/up pair, down)
     launch_groups = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
 
-    def layer_jobs(layer, wait_groups):
+    def layer_jobs(layer, wait_groups, xs_=None, ys_=None):
+        xs_ = xs if xs_ is None else xs_
+        ys_ = ys if ys_ is None else ys_
         jobs = []
         for gi, names in enumerate(launch_groups):
             for k, n in enumerate(names):
                 rows, cols, inp = shape[n]
-                jobs.append({"w": layer[n], "rows": rows, "cols": cols, "x": xs[inp], "y": ys[n],
+                jobs.append({"w": layer[n], "rows": rows, "cols": cols, "x": xs_[inp], "y": ys_[n],
                              "wait": wait_groups and gi > 0 and k == 0})
         return jobs
 
-    # Headline: each step is one pass over the seven matrices of the decode
-    # linear set, each with its own input (the workload's N(0,1) inputs are
-    # independent); steps go to q4k_gemv_seq in launches of STEPS_PER_LAUNCH
-    # sets, rotating over the layer copies so that no step finds its weights
-    # in L2.  One persistent launch streams all their weights.
-    ws_seq = None
+    ws_seq = {}   # one workspace per batch, shared by the lists of that batch (never run concurrently)
 
-    def seq_calls(first, count, per_launch=STEPS_PER_LAUNCH, wait_groups=False):
-        nonlocal ws_seq
-        calls = []
-        for c0 in range(first, first + count, per_launch):
+    def gemv_seq(jobs, batch=1):
+        try:
+            seq = q4k.GemvSeq(jobs, batch, workspace=ws_seq.get(batch))
+        except ValueError:                      # the shared workspace is too small for this list
+            seq = q4k.GemvSeq(jobs, batch)
+        if batch not in ws_seq or seq.workspace.numel() > ws_seq[batch].numel():
+            ws_seq[batch] = seq.workspace
+        return seq
+
+    def seq_calls(first, count, max_per=MAX_SETS_PER_LAUNCH, wait_groups=False):
+        calls, i = [], first
+        for n in even_split(count, max_per):
             jobs = []
-            for i in range(c0, min(first + count, c0 + per_launch)):
-                jobs += layer_jobs(copies[i % n_copies], wait_groups)
-            seq = q4k.GemvSeq(jobs, 1, workspace=ws_seq)
-            ws_seq = seq.workspace if ws_seq is None or seq.workspace.numel() > ws_seq.numel() else ws_seq
-            calls.append(seq)
+            for k in range(i, i + n):
+                jobs += layer_jobs(copies[k % n_copies], wait_groups)
+            calls.append(gemv_seq(jobs))
+            i += n
         return calls
 
-    def graph_of(calls):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for c in calls:
-                c()
-        return g
-
-    def time_graph(g):
-        g.replay()
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        t0.record()
-        g.replay()
-        t1.record()
-        barrier()
-        return t0.elapsed_time(t1)
-
+    # ---------------- headline: `steps` decode sets per replay
     warm_calls = seq_calls(0, args.warmup)
     timed_calls = seq_calls(args.warmup, args.steps)
-    n_launch_total = len(timed_calls)
+    n_launch = len(timed_calls)
     for c in warm_calls:
         c()
     torch.cuda.synchronize()
-    warm_graph = graph_of(warm_calls)
-    timed_graph = graph_of(timed_calls)
+    warm_graph = capture(lambda: [c() for c in warm_calls])
+    timed_graph = capture(lambda: [c() for c in timed_calls])
     warm_graph.replay()
+    ms_guess = time_graph(timed_graph, 3)
+    reps = max(MIN_REPLAYS, int(REPLAY_SECONDS * 1e3 / max(ms_guess, 1e-3)))
     sampler = ClockSampler(uuid)
     sampler.start()
-    time.sleep(0.3)
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    time.sleep(0.25)                      # the sampler's first reading is not part of the region
+    evs = [(ev(), ev()) for _ in range(reps)]
     barrier()
-    start.record()
-    timed_graph.replay()
-    stop.record()
+    sampler.mark(True)
+    for a, b in evs:
+        a.record()
+        timed_graph.replay()
+        b.record()
     barrier()
-    elapsed_ms = start.elapsed_time(stop)
-    # keep the same replays running long enough to sample clocks under load
-    t_end = time.perf_counter() + 2.0
-    while time.perf_counter() < t_end:
-        for _ in range(10):
-            timed_graph.replay()
-        torch.cuda.synchronize()
+    sampler.mark(False)
     clocks = sampler.stop()
+    replay_ms = sorted(a.elapsed_time(b) for a, b in evs)
+    elapsed_ms = statistics.median(replay_ms)
     if q4k.q4k_device_error() != 0:
         raise RuntimeError("a GEMV kernel gave up a bounded wait during the timed region")
 
     # ---------------- decode in engine order (each group reads the previous
-    # group's output): the 4-launch path and one q4k_gemv_seq per layer with waits
+    # group's output): one layer as 4 launches, one layer as one q4k_gemv_seq
+    # launch with waits, and the 36-layer token as q4k_gemv_seq launches
     def decode_step_4launch(i):
         layer = copies[i % n_copies]
         for names in launch_groups:
@@ -391,43 +476,52 @@ def run_ours(args, rank, world):
             else:
                 q4k.q4k_gemv_multi([layer[n] for n in names], rows, cols, xs[inp], ys=[ys[n] for n in names])
 
-    g4 = torch.cuda.CUDAGraph()
     for i in range(3):
         decode_step_4launch(i)
     torch.cuda.synchronize()
-    with torch.cuda.graph(g4):
-        for i in range(args.steps):
-            decode_step_4launch(i)
-    ms_4launch = time_graph(g4)
-    chain_calls = seq_calls(0, args.steps, per_launch=1, wait_groups=True)
+    ms_4launch = time_graph(capture(lambda: [decode_step_4launch(i) for i in range(args.steps)]), 20)
+    chain_calls = seq_calls(0, args.steps, max_per=1, wait_groups=True)
     for c in chain_calls[:3]:
         c()
-    ms_chain = time_graph(graph_of(chain_calls))
+    ms_chain = time_graph(capture(lambda: [c() for c in chain_calls]), 20)
 
-    # ---------------- 36-layer Qwen3-4B-shaped stack, one decode token per step
-    stack = {}
-    for sb in (1, 4):
-        xs_b = {name: torch.from_numpy(synth.activations(sb, cols, synth.layer_seed(synth.WL_STACK_4B, 0, 100 + j)))
+    def stack_token(batch, wait_groups):
+        """One decode token over the 36-layer stack (layer L reads copy L %
+        n_copies): 252 jobs, 3 launches."""
+        xs_b = {name: torch.from_numpy(synth.activations(batch, cols, synth.layer_seed(synth.WL_STACK_4B, 0, 100 + j)))
                 .to(dev) for j, (name, cols) in enumerate(synth.QWEN3_4B_INPUTS)}
-        ys_b = {n: torch.empty((sb, shape[n][0]), device=dev) for n in shape}
+        ys_b = {n: torch.empty((batch, shape[n][0]), device=dev) for n in shape}
         jobs = []
         for L in range(36):
-            layer = copies[L % n_copies]
-            for n in shape:
-                rows, cols, inp = shape[n]
-                jobs.append({"w": layer[n], "rows": rows, "cols": cols, "x": xs_b[inp], "y": ys_b[n]})
-        tok = q4k.GemvSeq(jobs, sb)
+            lj = layer_jobs(copies[L % n_copies], wait_groups, xs_b, ys_b)
+            lj[0]["wait"] = wait_groups and L > 0      # layer L's QKV reads layer L-1's output
+            jobs += lj
+        tok = gemv_seq(jobs, batch)
         tok()
         torch.cuda.synchronize()
         n_tok = 10
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(n_tok):
-                tok()
-        ms = time_graph(g)
-        stack[f"batch{sb}"] = {"tokens_per_s": sb * n_tok / (ms * 1e-3),
-                               "GB/s": 36 * layer_bytes * n_tok / (ms * 1e-3) / 1e9,
-                               "ms_per_token_step": ms / n_tok}
+        ms = time_graph(capture(lambda: [tok() for _ in range(n_tok)]), 10) / n_tok
+        return {"tokens_per_s": batch / (ms * 1e-3), "ms_per_token": ms,
+                "GB/s": 36 * set_bytes(batch) / (ms * 1e-3) / 1e9}
+
+    token_engine = {f"batch{b}": stack_token(b, True) for b in (1, 4)}
+    stack_indep = {f"batch{b}": stack_token(b, False) for b in (1, 4)}
+
+    # ---------------- single 2048x2048 GEMV, batch 1 (L2-resident: latency)
+    f0, x0 = synth.single_gemv_2048(0)
+    d0 = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev) for k, v in f0.items()}
+    w0 = q4k.q4k_pack(d0["d"], d0["dmin"], d0["sc"], d0["m"], d0["q"])
+    x0d = torch.from_numpy(x0).to(dev)
+    y0 = torch.empty((1, 2048), device=dev)
+    q4k.q4k_gemv(w0, 2048, 2048, x0d, y=y0)
+    torch.cuda.synchronize()
+    n_small = 100
+    us_gemv = 1e3 * time_graph(capture(lambda: [q4k.q4k_gemv(w0, 2048, 2048, x0d, y=y0) for _ in range(n_small)]),
+                               10) / n_small
+    seq0 = gemv_seq([{"w": w0, "rows": 2048, "cols": 2048, "x": x0d, "y": y0}])
+    seq0()
+    us_seq0 = 1e3 * time_graph(capture(lambda: [seq0() for _ in range(n_small)]), 10) / n_small
+    bytes0 = 2048 * 2048 * BYTES_PER_WEIGHT + 2 * 2048 * 4
 
     # ---------------- e2e: public API with host buffers, copies in the region
     inputs_host = {k: torch.from_numpy(v).pin_memory() for k, v in xs_np.items()}
@@ -435,19 +529,19 @@ def run_ours(args, rank, world):
                     for name, rows, _, _ in synth.QWEN3_4B_LAYER}
     h2d = sum(t.numel() * 4 for t in inputs_host.values())
     d2h = sum(t.numel() * 4 for t in outputs_host.values())
-    e2e_calls = seq_calls(0, args.warmup + args.steps, per_launch=1)
+    e2e_calls = seq_calls(0, args.warmup + args.steps, max_per=1)
 
     def e2e_step(i):
         for k_, t in inputs_host.items():
             xs[k_].copy_(t, non_blocking=True)
-        e2e_calls[i]()   # one q4k_gemv_seq call per step through the public API
+        e2e_calls[i]()   # one planned q4k_gemv_seq launch per step through the public API
         for name, t in outputs_host.items():
             t.copy_(ys[name], non_blocking=True)
 
     for i in range(args.warmup):
         e2e_step(i)
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = ev(), ev()
     e0.record()
     for i in range(args.steps):
         e2e_step(args.warmup + i)
@@ -455,71 +549,68 @@ def run_ours(args, rank, world):
     barrier()
     e2e_ms = e0.elapsed_time(e1)
 
-    # ---------------- prefill leg: q8_1 + MMQ GEMM, 512 tokens
+    # ---------------- prefill GEMMs (q8_1 + MMQ)
+    def prefill_case(mats, xs_in, tokens, layers=1, rotate=True):
+        """mats: [(name, fields, rows, cols, input)].  Times one step = q8_1 of
+        every input + every GEMM, `layers` times over rotating weight copies."""
+        w = {}
+        for name, f, rows, cols, inp in mats:
+            d = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev) for k, v in f.items()}
+            w[name] = q4k.q4k_pack(d["d"], d["dmin"], d["sc"], d["m"], d["q"])
+        x = {k: torch.from_numpy(v).to(dev) for k, v in xs_in.items()}
+        wbytes = sum(v.numel() for v in w.values())
+        n_c = max(2, math.ceil(4 * l2 / wbytes)) if rotate else 1
+        wsets = [w] + [{k: v.clone() for k, v in w.items()} for _ in range(n_c - 1)]
+        q8 = {k: q4k.q8_quantize(v) for k, v in x.items()}
+        y = {name: torch.empty((tokens, rows), device=dev) for name, _, rows, _, _ in mats}
+
+        def step(gemm_only=False):
+            for L in range(layers):
+                ws = wsets[L % n_c]
+                if not gemm_only:
+                    for k, v in x.items():
+                        q4k.q8_quantize(v, *q8[k])
+                for name, _, rows, cols, inp in mats:
+                    q4k.q4k_gemm(ws[name], rows, cols, *q8[inp], y=y[name])
+
+        step()
+        torch.cuda.synchronize()
+        ops = layers * sum(2.0 * tokens * rows * cols for _, _, rows, cols, _ in mats)
+        reps = 3 if layers > 1 else 10
+        ms = time_graph(capture(step), reps)
+        ms_gemm = time_graph(capture(lambda: step(True)), reps)
+        launches = layers * (len(x) + len(mats))
+        del wsets, w
+        return {"tokens": tokens, "ms_per_step": ms, "tok_s": tokens / (ms * 1e-3),
+                "int_tops": ops / (ms * 1e-3) / 1e12, "gemm_ms": ms_gemm,
+                "gemm_tops": ops / (ms_gemm * 1e-3) / 1e12, "gemm_frac_of_bf16": ops / (ms_gemm * 1e-3) / 1e12 / bf16,
+                "gpu_launches": launches, "l2": f"{n_c} rotating weight copies"}
+
     pf, pxs = synth.prefill_4b_512()
-    pw = {}
-    for name in ("gate", "down"):
-        d = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev)
-             for k, v in pf[name].items()}
-        pw[name] = q4k.q4k_pack(d["d"], d["dmin"], d["sc"], d["m"], d["q"])
-    px = {k: torch.from_numpy(v).to(dev) for k, v in pxs.items()}
-    pbytes = sum(v.numel() for v in pw.values()) + sum(v.numel() * 4 for v in px.values())
-    p_copies = max(2, math.ceil(4 * l2 / pbytes))
-    prefill_sets = [(pw, px)] + [({k: v.clone() for k, v in pw.items()}, {k: v.clone() for k, v in px.items()})
-                                 for _ in range(p_copies - 1)]
-    T = 512
-    pq = {"mlp_in": q4k.q8_quantize(px["mlp_in"]), "down_in": q4k.q8_quantize(px["down_in"])}
-    py = {"gate": torch.empty((T, 9728), device=dev), "down": torch.empty((T, 2560), device=dev)}
-    shapes = {"gate": (9728, 2560, "mlp_in"), "down": (2560, 9728, "down_in")}
+    mats512 = [("gate", pf["gate"], 9728, 2560, "mlp_in"), ("down", pf["down"], 2560, 9728, "down_in")]
+    prefill512 = prefill_case(mats512, pxs, 512)
+    prefill512["workload"] = "512-token prefill: q8_1 X[512x2560] x gate 9728x2560, X_down[512x9728] x down 2560x9728"
+    # short prompts (the pages' 18-33-token regime) on the same two matrices
+    short = {}
+    for T in (8, 16, 33, 64):
+        sx = {k: np.ascontiguousarray(v[:T]) for k, v in pxs.items()}
+        r = prefill_case(mats512, sx, T)
+        short[f"tokens{T}"] = {k: r[k] for k in ("ms_per_step", "tok_s", "gemm_tops", "gemm_frac_of_bf16")}
+    # 2048-token prefill of the 36-layer Qwen3-4B stack (7 projections a layer)
+    x2048 = {name: synth.activations(2048, cols, synth.layer_seed(synth.WL_STACK_4B, 0, 300 + j))
+             for j, (name, cols) in enumerate(synth.QWEN3_4B_INPUTS)}
+    mats_layer = [(n, fields[n], shape[n][0], shape[n][1], shape[n][2]) for n in shape]
+    prefill2048 = prefill_case(mats_layer, x2048, 2048, layers=36)
+    prefill2048["workload"] = ("2048-token prefill of the 36-layer Qwen3-4B-shaped stack: per layer q8_1 of 4 inputs "
+                               "and 7 GEMMs (q 4096x2560, k/v 1024x2560, o 2560x4096, gate/up 9728x2560, down 2560x9728)")
+    del x2048
+    # 4096-token prefill of the Qwen3-8B MLP
+    f8, x8 = synth.prefill_8b_4096()
+    mats8 = [(n, f8[n], rows, cols, inp) for n, rows, cols, inp in synth.QWEN3_8B_MLP]
+    prefill8b = prefill_case(mats8, x8, 4096)
+    prefill8b["workload"] = "4096-token prefill, Qwen3-8B MLP: gate/up 12288x4096, down 4096x12288"
+    del f8, x8
 
-    def prefill_step(i):
-        wset, xset = prefill_sets[i % p_copies]
-        for name in ("gate", "down"):
-            rows, cols, inp = shapes[name]
-            q, d8, s = pq[inp]
-            q4k.q8_quantize(xset[inp], q, d8, s)
-            q4k.q4k_gemm(wset[name], rows, cols, q, d8, s, y=py[name])
-
-    def gemm_only(i):
-        wset, _ = prefill_sets[i % p_copies]
-        for name in ("gate", "down"):
-            rows, cols, inp = shapes[name]
-            q, d8, s = pq[inp]
-            q4k.q4k_gemm(wset[name], rows, cols, q, d8, s, y=py[name])
-
-    for i in range(args.warmup):
-        prefill_step(i)
-    torch.cuda.synchronize()
-
-    def capture_fn(fn, first, count):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(first, first + count):
-                fn(i)
-        return g
-
-    pwarm = capture_fn(prefill_step, 0, args.warmup)
-    ptimed = capture_fn(prefill_step, args.warmup, args.steps)
-    gwarm = capture_fn(gemm_only, 0, args.warmup)
-    gtimed = capture_fn(gemm_only, args.warmup, args.steps)
-    pwarm.replay()
-    barrier()
-    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    p0.record()
-    ptimed.replay()
-    p1.record()
-    barrier()
-    prefill_ms = p0.elapsed_time(p1)
-    # the GEMM launches alone (same inputs), for the GEMM's own roofline
-    gwarm.replay()
-    torch.cuda.synchronize()
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record()
-    gtimed.replay()
-    g1.record()
-    torch.cuda.synchronize()
-    gemm_ms = g0.elapsed_time(g1)
-    gemm_ops = 2.0 * T * (9728 * 2560 + 2560 * 9728)
     # tensor-core rate probes on this GPU: the int8 rate of the warp-level
     # MMA (mma.sync m16n8k32 s8) and the fp16 rate of tcgen05.mma kind::f16
     from q4_weight_matmul_gb300 import peaks as tc_peaks
@@ -532,7 +623,6 @@ def run_ours(args, rank, world):
 
     elapsed_ms = max_over_ranks(elapsed_ms)
     e2e_ms = max_over_ranks(e2e_ms)
-    prefill_ms = max_over_ranks(prefill_ms)
 
     if rank != 0:
         if dist is not None:
@@ -541,68 +631,87 @@ def run_ours(args, rank, world):
 
     value = job_throughput(step_bytes, args.steps, world, elapsed_ms)
     e2e_value = job_throughput(step_bytes, args.steps, world, e2e_ms)
-    # the timed region holds nothing but this kernel's launches: its average
-    # launch duration is the region over the launches, and each launch
-    # processes STEPS_PER_LAUNCH steps' algorithmic bytes
+    # the timed replay holds nothing but this kernel's launches: the average
+    # launch duration is the replay over its launches, and each launch
+    # processes its sets' algorithmic bytes
     achieved = step_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
-    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    traffic = profile_traffic("gemv_seq", "gemv_seq.cu")
-    bf16 = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
-    gemm_tops = gemm_ops * args.steps / (gemm_ms * 1e-3) / 1e12
+    traffic_rec = profile_traffic("gemv_seq", ["gemv_seq.cu", "gemv_common.cuh"])
+    traffic = None
+    if traffic_rec is not None:
+        # the record is for a launch of MAX_SETS_PER_LAUNCH sets: scale to this run's average launch
+        traffic = traffic_rec * (args.steps / n_launch) / MAX_SETS_PER_LAUNCH
 
     cpu = None
+    cpu_single = None
+    cpu_gemm = None
     if world == 1 and not args.no_cpu_baseline:
         gbs, spent, desc = oracle_decode_sample(args.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": desc,
                "seconds": round(spent, 2)}
+        cpu_single = single_core_decode(args.cpu_seconds)
+        tops, tok_s, spent, desc = oracle_gemm_sample(args.cpu_seconds)
+        cpu_gemm = {"value": tok_s, "unit": "tok/s", "int_tops": tops, "cores": cpu_threads(), "kind": "oracle",
+                    "sample": desc, "seconds": round(spent, 2)}
 
+    sm_mhz = (clocks or {}).get("sm_mhz")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "parallelism": "replicas" if world > 1 else "single",
-                   "timing": f"one CUDA graph of exactly `steps` steps; each step is the seven GEMVs of the "
-                             f"decode linear set (independent N(0,1) inputs), {STEPS_PER_LAUNCH} steps per "
-                             f"q4k_gemv_seq launch",
+                   "timing": (f"median of {reps} back-to-back replays of one CUDA graph of exactly `steps` steps "
+                              f"(replay times: min {replay_ms[0]:.4f} ms, median {elapsed_ms:.4f} ms, "
+                              f"max {replay_ms[-1]:.4f} ms); each step is the seven GEMVs of the decode linear "
+                              f"set (independent N(0,1) inputs); the steps are split evenly over "
+                              f"{n_launch} q4k_gemv_seq launches ({even_split(args.steps, MAX_SETS_PER_LAUNCH)} "
+                              f"sets)"),
                    "l2": f"inputs larger than L2: {n_copies} rotating layer copies "
                          f"({n_copies * layer_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
-                   "launches": n_launch_total},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "peak_kind": f"{peak_kind} hbm_gbs",
+                   "launches": n_launch},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
+                     "traffic": traffic, "peak_kind": f"{peak_kind} hbm_gbs",
                      "kernel": "gemv_seq_kernel<1>",
-                     "duration": "CUDA events on the launching stream around the timed region (one graph "
-                                 "of the launches of this kernel, nothing else), divided by its launches; "
-                                 "algorithmic bytes per launch = the steps it holds x bytes per step"},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": n_launch_total,
+                     "duration": "CUDA events on the launching stream around each replay (one graph of the "
+                                 "launches of this kernel, nothing else), divided by its launches; algorithmic "
+                                 "bytes per launch = the sets it holds x bytes per set"},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "per step: pinned host inputs to the device, one q4k_gemv_seq_launch of a prepared plan, "
+                        "outputs back to pinned host memory; no graph"},
+        "gpu_launches": n_launch,
         "clocks": clocks,
+        "time_x_sm_mhz": (elapsed_ms / args.steps * 1e3 * sm_mhz) if sm_mhz else None,
         "decode_engine_order": {
             "note": "each input group reads the previous group's output (QKV | o | gate,up | down)",
-            "4_launches_per_layer": {"us_per_layer": 1e3 * ms_4launch / args.steps,
-                                     "GB/s": step_bytes * args.steps / (ms_4launch * 1e-3) / 1e9},
-            "gemv_seq_one_launch_per_layer_with_waits": {
-                "us_per_layer": 1e3 * ms_chain / args.steps,
-                "GB/s": step_bytes * args.steps / (ms_chain * 1e-3) / 1e9}},
-        "decode_stack_36_layers": stack,
+            "layer_4_launches": {"us_per_layer": 1e3 * ms_4launch / args.steps,
+                                 "GB/s": step_bytes * args.steps / (ms_4launch * 1e-3) / 1e9},
+            "layer_gemv_seq_with_waits": {"us_per_layer": 1e3 * ms_chain / args.steps,
+                                          "GB/s": step_bytes * args.steps / (ms_chain * 1e-3) / 1e9},
+            "token_36_layers_gemv_seq_with_waits": token_engine},
+        "decode_stack_36_layers_independent_jobs": {
+            "note": "the 252 GEMVs of the stack with no dependencies between them (not a decode token)",
+            **stack_indep},
+        "single_gemv_2048x2048_b1": {"us_q4k_gemv": us_gemv, "us_gemv_seq": us_seq0,
+                                     "GB/s_q4k_gemv": bytes0 / (us_gemv * 1e-6) / 1e9,
+                                     "note": "2.4 MB of weights, L2-resident: a latency case"},
         "cpu_baseline": cpu,
+        "cpu_baseline_single_core": cpu_single,
+        "cpu_baseline_gemm_prefill512": cpu_gemm,
         "pack": {"ms": pack_ms, "GB/s": pack_bytes / (pack_ms * 1e-3) / 1e9, "note": "one-off, 7 matrices"},
         "prefill": {
-            "workload": PREFILL_WORKLOAD, "tokens": T,
-            "ms_per_step": prefill_ms / args.steps,
-            "tok_s": T * args.steps * world / (prefill_ms * 1e-3),
-            "int_tops": gemm_ops * args.steps * world / (prefill_ms * 1e-3) / 1e12,
-            "gemm_tops": gemm_tops,
-            # the GEMM's MMAs are tcgen05 kind::f16 (exact small integers in
-            # fp16), so its own-dtype peak is the dense fp16 = bf16 rate
-            "roofline": {"bound": "tensor", "achieved": gemm_tops, "unit": "TOPS", "peak": bf16,
-                         "frac": gemm_tops / bf16, "peak_kind": f"{peak_kind} bf16_tflops (fp16 rate)",
-                         "int8_peak_mma_sync_s8": int8_peak, "frac_of_int8_peak": gemm_tops / int8_peak,
+            **prefill512,
+            "roofline": {"bound": "tensor", "achieved": prefill512["gemm_tops"], "unit": "TOPS", "peak": bf16,
+                         "frac": prefill512["gemm_tops"] / bf16, "peak_kind": f"{peak_kind} bf16_tflops (fp16 rate)",
+                         "note": "the GEMM's MMAs are tcgen05 kind::f16 on exact small integers, so its own-dtype "
+                                 "peak is the dense fp16 = bf16 rate; sm_103a has no integer tcgen05 MMA",
+                         "int8_peak_mma_sync_s8": int8_peak, "frac_of_int8_peak": prefill512["gemm_tops"] / int8_peak,
                          "tcgen05_f16_probe_tflops": f16_peak},
-            "gpu_launches": 4 * args.steps,
-            "timing": "one CUDA graph of exactly `steps` steps (q8_1 + GEMM for gate and down); "
+            "timing": "median of CUDA-graph replays of exactly one step (q8_1 + GEMM for gate and down); "
                       "gemm_tops from a graph of the GEMM launches alone",
-            "l2": f"{p_copies} rotating weight+input copies",
         },
+        "prefill_short_prompts": short,
+        "prefill_2048_stack": prefill2048,
+        "prefill_4096_qwen3_8b_mlp": prefill8b,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:
@@ -613,11 +722,11 @@ def run_ours(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=52)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -22,6 +22,23 @@
  *    Activations are [tokens][cols], outputs are [tokens][rows].
  *  - Device pointers must be 16-byte aligned (Q4K_ERR_ALIGNMENT otherwise).
  *  - Sizes of zero (rows, tokens, batch) are valid and enqueue nothing.
+ *  - A call whose work takes more than one kernel launch (a q4k_gemv_seq
+ *    list of more than 96 jobs) validates and plans all of it first; only a
+ *    CUDA launch failure of a later launch can leave the earlier ones
+ *    enqueued (the status is then Q4K_ERR_CUDA).
+ *
+ * Accuracy of every fp32 output (decode GEMV and prefill GEMM).  The kernels
+ * apply the scale term d*sc*q and the min term dmin*m of each weight as
+ * separate sums, as the MMQ form does, so their rounding is bounded against
+ *     M = sum_k (|d*sc*q_k| + |dmin*m_k|) * |x_k|   (+ |residual|):
+ *     |y - exact| <= 1e-4 * M,
+ * where x is the fp32 activation (GEMV) or the dequantised q8_1 activation
+ * d8*q8 (GEMM).  M equals sum_k |w_k||x_k| except where the two terms of a
+ * weight cancel, and the bound is then also 1e-4 * sum_k |w_k||x_k|
+ * whenever M <= 1.5 * sum_k |w_k||x_k|.  The bound holds for finite inputs
+ * whose nonzero products |d*sc*q*x|, |dmin*m*x| and results lie between
+ * 2^-100 and 2^100 (nearer fp32's underflow or overflow, its own rounding
+ * there bounds the error instead).
  *
  * The Q4_K superblock (genie-ai-runtime §2 "Qwen3-4B Q4_K_M weights"; the
  * pages name the format but print no byte layout, so the common GGUF Q4_K
@@ -54,15 +71,32 @@ typedef enum q4k_status {
 } q4k_status;
 
 typedef enum q4k_layout {
-  Q4K_LAYOUT_BLOCK144 = 0     /* 144-byte superblocks, GGUF byte order     */
+  Q4K_LAYOUT_BLOCK144 = 0,    /* 144-byte superblocks, GGUF byte order     */
+  Q4K_LAYOUT_GPU = 1          /* reserved: rows interleaved for vector
+                                 loads; every call returns
+                                 Q4K_ERR_UNSUPPORTED (see below)           */
 } q4k_layout;
 
+/*
+ * Q4K_LAYOUT_GPU is the row-interleaved repack that CPU kernels use to load
+ * several rows per vector ("I'm making LLMs work on small and old devices":
+ * the llama.cpp repack of row counts divisible by 8).  This library does not
+ * build it: its kernels copy BLOCK144 weights with 3-D tensor copies whose
+ * boxes already regroup rows (row r of a 32-row box is 144 bytes from row
+ * r+1 in shared memory), so an interleaved copy in device memory would gain
+ * nothing and cost a second layout.
+ */
+
 /* Bytes of a packed rows x cols weight matrix in `layout`
- * (rows * cols/256 * 144 for BLOCK144); 0 for an invalid request. */
+ * (rows * cols/256 * 144 for BLOCK144); 0 for an invalid or unsupported
+ * request.  (genie-ai-runtime §2: Qwen3-4B Q4_K_M weights, ~2.3 GB, are
+ * what every decode step streams.) */
 size_t q4k_packed_bytes(int64_t rows, int64_t cols, int layout);
 
 /*
- * q4k_pack - pack Q4_K fields into superblocks (the packer/layout step).
+ * q4k_pack - pack Q4_K fields into superblocks (the packer/layout step;
+ * genie-ai-runtime §2 names the Q4_K_M format the engine runs; the byte
+ * order is the one described at the top of this header).
  *   d, dmin : uint16 binary16 bits, [rows][cols/256]
  *   sc, m   : uint8 values 0..63,   [rows][cols/32]   (bits above 5 ignored)
  *   q       : uint8 values 0..15,   [rows][cols]      (bits above 3 ignored)
@@ -74,7 +108,27 @@ int q4k_pack(const uint16_t* d, const uint16_t* dmin, const uint8_t* sc,
              int layout, void* w, void* stream);
 
 /*
- * q8_quantize - fp32 activations to q8_1 blocks of 32 (prefill input).
+ * q4k_unpack - test export, the inverse of q4k_pack: read every field back
+ * out of packed superblocks (same arrays and shapes as q4k_pack; sc, m and q
+ * come back in their low 6 / 6 / 4 bits with the bits above them zero).
+ * Bit-exact: q4k_unpack(q4k_pack(f)) == f for fields within their ranges.
+ */
+int q4k_unpack(const void* w, int layout, int64_t rows, int64_t cols,
+               uint16_t* d, uint16_t* dmin, uint8_t* sc, uint8_t* m,
+               uint8_t* q, void* stream);
+
+/*
+ * q8_1_bytes - device bytes of the q8_1 form of a tokens x cols activation
+ * matrix: q (1 byte per element) plus d8 and sum (4 bytes each per 32
+ * elements), whether kept in one buffer or three; 0 for an invalid request.
+ */
+size_t q8_1_bytes(int64_t tokens, int64_t cols);
+
+/*
+ * q8_quantize - fp32 activations to q8_1 blocks of 32 (prefill input: the
+ * integer activation blocks of the MMQ form; genie-ai-runtime §3 Path E is
+ * the batched Q4_K prefill kernel these feed; the pages do not print the
+ * block, so its definition is this one).
  * For each row t and each block b of 32 consecutive columns:
  *   amax = max |x|, d8 = amax / 127 (IEEE fp32 division),
  *   q = clamp(roundf(x / d8), -127, 127) (fp32 division, ties away from 0),
@@ -96,11 +150,14 @@ int q8_quantize(const float* x, int64_t tokens, int64_t cols, int8_t* q,
  *   x        : float [batch][cols], 1 <= batch <= 8
  *   residual : float [batch][rows] or NULL
  *   y        : float [batch][rows]; may alias residual, not x or w
- * Accuracy: |y - exact| <= 1e-4 * sum_k |w||x| (+|residual|) per element.
- * Arithmetic: each 32-wide block of x is held as a 23-bit fixed-point
- * integer with a power-of-two scale (error <= 2^-22 of the block's largest
- * |x| per element), the quant-times-x block sums are exact integers, and the
- * scales d*sc, dmin*m are applied in fp32.
+ * Accuracy: the bound at the top of this header, per element.
+ * Arithmetic: each 32-wide block of x is held as a 32-bit fixed-point
+ * integer with a power-of-two scale, the quant-times-x block sums are exact
+ * integers, and the scales d*sc, dmin*m are applied in fp32.  Blocks where
+ * 24 bits keep every element within 2^-14 of itself use three byte planes,
+ * blocks that need more add a fourth, and blocks that 32 bits cannot hold
+ * that closely (an element below ~2^-16 of the block's largest, or a
+ * largest |x| outside [2^-87, 2^94)) are summed in fp32.
  * Deterministic: the same inputs give the same bits on every run.
  */
 int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols,
@@ -170,7 +227,7 @@ size_t q4k_gemv_seq_workspace_bytes(const q4k_gemv_job* jobs, int n_jobs, int64_
  *               share a workspace must not overlap on the GPU.
  * The launch is cooperative (every CTA resident at once, one per SM); it
  * fails with Q4K_ERR_CUDA when the GPU cannot hold them all.
- * Accuracy as q4k_gemv: |y - exact| <= 1e-4 * sum_k |w||x| (+|residual|).
+ * Accuracy and arithmetic as q4k_gemv.
  * Deterministic: for one job list on one device, the same inputs give the
  * same bits on every run.
  * Errors: Q4K_ERR_INVALID_ARG (null pointer, bad size, workspace too small),
@@ -179,6 +236,32 @@ size_t q4k_gemv_seq_workspace_bytes(const q4k_gemv_job* jobs, int n_jobs, int64_
  */
 int q4k_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch,
                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * q4k_gemv_seq_plan / q4k_gemv_seq_launch - q4k_gemv_seq split into a
+ * planning step done once and a launch done every step, for an engine that
+ * runs the same job list with the same buffers every decode step (the pages'
+ * engine pre-allocates its pools and does no allocation or set-up on the
+ * hot path, genie-ai-runtime §4 "Memory-first").
+ *   plan_bytes = q4k_gemv_seq_plan_bytes(n_jobs): host bytes of a plan
+ *     (about 32 KB per 96 jobs); 0 if n_jobs is out of range.
+ *   q4k_gemv_seq_plan validates the list exactly as q4k_gemv_seq does and
+ *     writes the plan (tensor maps of every weight matrix, the work split,
+ *     every device pointer of the jobs and the workspace) into `plan`:
+ *     caller-owned HOST memory of at least plan_bytes bytes, 64-byte
+ *     aligned (Q4K_ERR_ALIGNMENT otherwise).  It enqueues nothing and
+ *     allocates nothing; `workspace` is as for q4k_gemv_seq.
+ *   q4k_gemv_seq_launch enqueues the plan's launches on `stream`: the same
+ *     work, results and accuracy as the q4k_gemv_seq call the plan was made
+ *     from.  The pointers baked into the plan must stay valid, the plan must
+ *     not be changed, and launches from one plan (or of plans sharing a
+ *     workspace) must not overlap on the GPU.  Call it on the device that was
+ *     current when the plan was made (Q4K_ERR_INVALID_ARG otherwise).
+ */
+size_t q4k_gemv_seq_plan_bytes(int n_jobs);
+int q4k_gemv_seq_plan(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch,
+                      void* workspace, size_t workspace_bytes, void* plan, size_t plan_bytes);
+int q4k_gemv_seq_launch(const void* plan, void* stream);
 
 /*
  * q4k_gemv_seq_static - q4k_gemv_seq for callers that cannot allocate device
@@ -194,7 +277,9 @@ int q4k_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and keeps it; make that first call before any
  *    stream capture.
- *  - Each call first clears the array's counters on `stream`, then launches.
+ *  - Each call plans and checks the whole list first, then clears the
+ *    array's counters on `stream`, then launches; if that launch fails,
+ *    the clear (of the library's own array) is the one thing left enqueued.
  *  - All calls on a device share the one array: calls that overlap on the
  *    GPU (other streams, other host threads) race and give wrong results.
  *  - A job list whose scratch would exceed 1 MiB (the need grows with the
@@ -213,7 +298,7 @@ int q4k_gemv_seq_static(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_
  *   w         : packed weights (layout), rows x cols
  *   q8,d8,sum : q8_quantize() output for `tokens` rows of width cols
  *   y         : float [tokens][rows]
- * Accuracy: |y - exact| <= 1e-4 * sum_k |w| |d8 q8| per element.
+ * Accuracy: the bound at the top of this header, with x = d8*q8.
  */
 int q4k_gemm(const void* w, int layout, int64_t rows, int64_t cols,
              const int8_t* q8, const float* d8, const int32_t* sum,

@@ -17,6 +17,7 @@ import torch
 from .build import LIB_PATH, build
 
 BLOCK144 = 0
+LAYOUT_GPU = 1          # declared by the C ABI; every call refuses it (Q4K_ERR_UNSUPPORTED)
 Q4K_OK = 0
 QK_K = 256
 QK_SUB = 32
@@ -38,11 +39,16 @@ class GemvJob(ctypes.Structure):
 SIGNATURES = {
     "q4k_packed_bytes": (ctypes.c_size_t, [_I64, _I64, _I]),
     "q4k_pack": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _P, _P]),
+    "q4k_unpack": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _P, _P, _P]),
+    "q8_1_bytes": (ctypes.c_size_t, [_I64, _I64]),
     "q8_quantize": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q4k_gemv": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P, _P]),
     "q4k_gemv_multi": (_I, [_I, _P, _I, _P, _I64, _P, _I64, _P, _P, _P]),
     "q4k_gemv_seq_workspace_bytes": (ctypes.c_size_t, [_P, _I, _I64]),
     "q4k_gemv_seq": (_I, [_P, _I, _I, _I64, _P, ctypes.c_size_t, _P]),
+    "q4k_gemv_seq_plan_bytes": (ctypes.c_size_t, [_I]),
+    "q4k_gemv_seq_plan": (_I, [_P, _I, _I, _I64, _P, ctypes.c_size_t, _P, ctypes.c_size_t]),
+    "q4k_gemv_seq_launch": (_I, [_P, _P]),
     "q4k_gemv_seq_static": (_I, [_P, _I, _I, _I64, _P]),
     "q4k_gemm": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
     "q4k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
@@ -129,6 +135,27 @@ def q4k_pack(d, dmin, sc, m, q, out=None, layout: int = BLOCK144, stream=None):
     return out
 
 
+def q4k_unpack(w, rows: int, cols: int, layout: int = BLOCK144, stream=None):
+    """Test export: read the fields back out of packed weights; returns
+    ``{"d", "dmin"}`` (int16 tensors holding binary16 bits) and ``{"sc", "m", "q"}`` (uint8)."""
+    dev = w.device
+    nb = cols // QK_K
+    out = {"d": torch.empty((rows, nb), dtype=torch.int16, device=dev),
+           "dmin": torch.empty((rows, nb), dtype=torch.int16, device=dev),
+           "sc": torch.empty((rows, cols // QK_SUB), dtype=torch.uint8, device=dev),
+           "m": torch.empty((rows, cols // QK_SUB), dtype=torch.uint8, device=dev),
+           "q": torch.empty((rows, cols), dtype=torch.uint8, device=dev)}
+    _check(lib().q4k_unpack(_ptr(w, torch.uint8, "w"), layout, rows, cols,
+                            _ptr16(out["d"], "d"), _ptr16(out["dmin"], "dmin"),
+                            _ptr(out["sc"], torch.uint8, "sc"), _ptr(out["m"], torch.uint8, "m"),
+                            _ptr(out["q"], torch.uint8, "q"), _stream(stream)), "q4k_unpack")
+    return out
+
+
+def q8_1_bytes(tokens: int, cols: int) -> int:
+    return int(lib().q8_1_bytes(tokens, cols))
+
+
 def q8_quantize(x, q=None, d8=None, s=None, stream=None):
     """q8_1-quantise ``x`` [tokens][cols] float32; returns (q int8, d8 float32, sum int32)."""
     tokens, cols = x.shape
@@ -171,57 +198,10 @@ def q4k_gemv_multi(ws, rows, cols: int, x, residuals=None, ys=None, layout: int 
     return ys
 
 
-class GemvSeq:
-    """A prepared ``q4k_gemv_seq`` job list: the C job array and a zeroed
-    workspace, built once; calling it enqueues the one persistent launch.
-
-    ``jobs`` is a sequence of dicts with keys ``w`` (packed uint8), ``rows``,
-    ``cols``, ``x`` ([batch][cols] float32), ``y`` ([batch][rows] float32),
-    optional ``residual`` and ``wait`` (read x only after every earlier job
-    has stored its y).  The tensors must stay alive while the list is used.
-    """
-
-    def __init__(self, jobs, batch: int, layout: int = BLOCK144, workspace=None):
-        n = len(jobs)
-        arr = (GemvJob * max(n, 1))()
-        dev = None
-        for i, j in enumerate(jobs):
-            arr[i].w = _ptr(j["w"], torch.uint8, "w")
-            arr[i].rows = int(j["rows"])
-            arr[i].cols = int(j["cols"])
-            arr[i].x = _ptr(j["x"], torch.float32, "x")
-            arr[i].residual = _ptr(j.get("residual"), torch.float32, "residual")
-            arr[i].y = _ptr(j["y"], torch.float32, "y")
-            arr[i].wait = 1 if j.get("wait") else 0
-            dev = j["x"].device if dev is None else dev
-        self.jobs, self.n, self.batch, self.layout = arr, n, int(batch), layout
-        need = int(lib().q4k_gemv_seq_workspace_bytes(arr, n, self.batch)) if n else 0
-        if workspace is None:
-            workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
-        elif workspace.numel() < need:
-            raise ValueError(f"workspace holds {workspace.numel()} bytes, the job list needs {need}")
-        self.workspace = workspace
-        self.workspace_bytes = need
-
-    def __call__(self, stream=None):
-        _check(lib().q4k_gemv_seq(self.jobs, self.n, self.layout, self.batch,
-                                  _ptr(self.workspace, torch.uint8, "workspace"),
-                                  self.workspace.numel(), _stream(stream)), "q4k_gemv_seq")
-
-
-def q4k_gemv_seq(jobs, batch: int, layout: int = BLOCK144, workspace=None, stream=None):
-    """One persistent launch over an ordered GEMV job list (see ``GemvSeq``)."""
-    seq = GemvSeq(jobs, batch, layout, workspace)
-    seq(stream)
-    return seq
-
-
-def q4k_gemv_seq_static(jobs, batch: int, layout: int = BLOCK144, stream=None):
-    """``q4k_gemv_seq`` without a workspace: the library's built-in scratch
-    array serves instead, so nothing is allocated (for callers that cannot
-    allocate device memory).  Calls that overlap on the GPU race."""
+def _job_array(jobs):
     n = len(jobs)
     arr = (GemvJob * max(n, 1))()
+    dev = None
     for i, j in enumerate(jobs):
         arr[i].w = _ptr(j["w"], torch.uint8, "w")
         arr[i].rows = int(j["rows"])
@@ -230,6 +210,63 @@ def q4k_gemv_seq_static(jobs, batch: int, layout: int = BLOCK144, stream=None):
         arr[i].residual = _ptr(j.get("residual"), torch.float32, "residual")
         arr[i].y = _ptr(j["y"], torch.float32, "y")
         arr[i].wait = 1 if j.get("wait") else 0
+        dev = j["x"].device if dev is None else dev
+    return arr, n, dev
+
+
+def _workspace(arr, n, batch, dev, workspace):
+    need = int(lib().q4k_gemv_seq_workspace_bytes(arr, n, batch)) if n else 0
+    if workspace is None:
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+    elif workspace.numel() < need:
+        raise ValueError(f"workspace holds {workspace.numel()} bytes, the job list needs {need}")
+    return workspace, need
+
+
+class GemvSeq:
+    """A prepared ``q4k_gemv_seq`` job list: the C job array, a zeroed
+    workspace and the host plan (``q4k_gemv_seq_plan``), built once; calling
+    it enqueues the plan's persistent launch (``q4k_gemv_seq_launch``).
+
+    ``jobs`` is a sequence of dicts with keys ``w`` (packed uint8), ``rows``,
+    ``cols``, ``x`` ([batch][cols] float32), ``y`` ([batch][rows] float32),
+    optional ``residual`` and ``wait`` (read x only after every earlier job
+    has stored its y).  The tensors must stay alive while the list is used.
+    """
+
+    def __init__(self, jobs, batch: int, layout: int = BLOCK144, workspace=None):
+        arr, n, dev = _job_array(jobs)
+        self.jobs, self.n, self.batch, self.layout = arr, n, int(batch), layout
+        self.workspace, self.workspace_bytes = _workspace(arr, n, self.batch, dev, workspace)
+        nbytes = int(lib().q4k_gemv_seq_plan_bytes(n))
+        if nbytes == 0:
+            raise Q4KError(3, "q4k_gemv_seq_plan_bytes")
+        self._plan_buf = ctypes.create_string_buffer(nbytes + 64)
+        base = ctypes.addressof(self._plan_buf)
+        self.plan = base + (-base) % 64          # the plan must be 64-byte aligned
+        _check(lib().q4k_gemv_seq_plan(arr, n, layout, self.batch,
+                                       _ptr(self.workspace, torch.uint8, "workspace"),
+                                       self.workspace.numel(), self.plan, nbytes), "q4k_gemv_seq_plan")
+
+    def __call__(self, stream=None):
+        _check(lib().q4k_gemv_seq_launch(self.plan, _stream(stream)), "q4k_gemv_seq_launch")
+
+
+def q4k_gemv_seq(jobs, batch: int, layout: int = BLOCK144, workspace=None, stream=None):
+    """One call of ``q4k_gemv_seq`` (plan and launch in one) over an ordered
+    GEMV job list (see ``GemvSeq``); returns the workspace it used."""
+    arr, n, dev = _job_array(jobs)
+    workspace, _ = _workspace(arr, n, int(batch), dev, workspace)
+    _check(lib().q4k_gemv_seq(arr, n, layout, int(batch), _ptr(workspace, torch.uint8, "workspace"),
+                              workspace.numel(), _stream(stream)), "q4k_gemv_seq")
+    return workspace
+
+
+def q4k_gemv_seq_static(jobs, batch: int, layout: int = BLOCK144, stream=None):
+    """``q4k_gemv_seq`` without a workspace: the library's built-in scratch
+    array serves instead, so nothing is allocated (for callers that cannot
+    allocate device memory).  Calls that overlap on the GPU race."""
+    arr, n, _ = _job_array(jobs)
     _check(lib().q4k_gemv_seq_static(arr, n, layout, int(batch), _stream(stream)), "q4k_gemv_seq_static")
 
 
@@ -272,7 +309,8 @@ def q4k_version() -> str:
     return lib().q4k_version().decode()
 
 
-__all__ = ["build", "lib", "Q4KError", "BLOCK144", "q4k_packed_bytes", "q4k_pack", "q8_quantize",
+__all__ = ["build", "lib", "Q4KError", "BLOCK144", "LAYOUT_GPU", "q4k_packed_bytes", "q4k_pack", "q4k_unpack",
+           "q8_1_bytes", "q8_quantize",
            "q4k_gemv", "q4k_gemv_multi", "GemvJob", "GemvSeq", "q4k_gemv_seq", "q4k_gemv_seq_static", "q4k_gemm",
            "q4k_gemm_blockdots", "q4k_device_error",
            "q4k_selftest_wait_timeout", "q4k_version",

@@ -126,6 +126,25 @@ int q4k_pack(const uint16_t* d, const uint16_t* dmin, const uint8_t* sc,
   return e == cudaSuccess ? Q4K_OK : record_cuda(e);
 }
 
+size_t q8_1_bytes(int64_t tokens, int64_t cols) {
+  if (tokens < 0 || tokens > (int64_t(1) << 24) || check_cols(cols)) return 0;
+  return (size_t)tokens * (size_t)cols + 2 * sizeof(int32_t) * (size_t)tokens * (size_t)(cols / kSub);
+}
+
+int q4k_unpack(const void* w, int layout, int64_t rows, int64_t cols, uint16_t* d, uint16_t* dmin,
+               uint8_t* sc, uint8_t* m, uint8_t* q, void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_layout(layout)) return e;
+  if (rows == 0) return Q4K_OK;
+  if (!w || !d || !dmin || !sc || !m || !q) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(d) || !aligned16(dmin) || !aligned16(sc) || !aligned16(m) || !aligned16(q))
+    return Q4K_ERR_ALIGNMENT;
+  cudaError_t e = launch_unpack_block144(static_cast<const uint8_t*>(w), rows, cols, d, dmin, sc, m, q,
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
 int q8_quantize(const float* x, int64_t tokens, int64_t cols, int8_t* q, float* d8,
                 int32_t* sum, void* stream) {
   if (tokens < 0 || tokens > (int64_t(1) << 24)) return Q4K_ERR_INVALID_ARG;
@@ -264,6 +283,35 @@ int q4k_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch
   cudaError_t ce = cudaSuccess;
   const int st = launch_gemv_seq(jobs, n_jobs, (int)batch, workspace, workspace_bytes,
                                  static_cast<cudaStream_t>(stream), &ce);
+  if (st == Q4K_ERR_CUDA) return record_cuda(ce);
+  return st;
+}
+
+size_t q4k_gemv_seq_plan_bytes(int n_jobs) {
+  if (n_jobs < 0 || n_jobs > kGemvSeqMaxJobs) return 0;
+  return gemv_seq_plan_bytes(n_jobs);
+}
+
+int q4k_gemv_seq_plan(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch, void* workspace,
+                      size_t workspace_bytes, void* plan, size_t plan_bytes) {
+  bool work = false;
+  if (int e = check_seq(jobs, n_jobs, layout, batch, &work)) return e;
+  if (!plan) return Q4K_ERR_INVALID_ARG;
+  if (work) {
+    if (!workspace) return Q4K_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return Q4K_ERR_ALIGNMENT;
+  }
+  cudaError_t ce = cudaSuccess;
+  const int st = gemv_seq_plan(jobs, n_jobs, work ? (int)batch : 0, work ? workspace : nullptr,
+                               workspace_bytes, plan, plan_bytes, &ce);
+  if (st == Q4K_ERR_CUDA) return record_cuda(ce);
+  return st;
+}
+
+int q4k_gemv_seq_launch(const void* plan, void* stream) {
+  if (!plan) return Q4K_ERR_INVALID_ARG;
+  cudaError_t ce = cudaSuccess;
+  const int st = gemv_seq_launch(plan, static_cast<cudaStream_t>(stream), &ce);
   if (st == Q4K_ERR_CUDA) return record_cuda(ce);
   return st;
 }

@@ -27,8 +27,8 @@
 // chunk.  A chunk's 32 quant bytes hold sub-block 2c in low nibbles and 2c+1
 // in high nibbles.
 //
-// Arithmetic: 23-bit fixed-point activation planes and exact integer dp4a
-// block sums, scales applied in fp32 (gemv_common.cuh).
+// Arithmetic: 32-bit fixed-point activation digit planes and exact integer
+// dp4a block sums, scales applied in fp32 (gemv_common.cuh).
 #include "gemv_common.cuh"
 #include "q4k_internal.h"
 #include "tc_ptx.cuh"
@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
       tc::mbar_init(&empty[i], SB);
     }
     *issued = 0;
+    int* pc = gemv::pool_counter(xss);
+    pc[0] = pc[1] = pc[2] = pc[3] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -174,8 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
 
   // -------------------------------------------------------------- consumers
   if (P.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
-  gemv::stage_x<B, kConsumers, false>(P.x, nb, xs, xss, tid);
+  gemv::stage_x<B, kConsumers, false>(P.x, nb, xs, xss, tid, 0);
   named_sync_consumers();
+  const gemv::XView xv = gemv::make_view(xs, xss, P.x, B, nb);
 
   const int r_in = lane / LPR;              // row inside the block
   const int lq = lane % LPR;                // this lane's share of the superblock
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
       if (sb < nb) {
         // stage laid out [SB][RB][144] (rows inner)
         const uint8_t* p = stages + (size_t)slot * kStageBytes + ((size_t)z * RB + r_in) * kBlockBytes;
-        gemv::superblock_dot<B, CPL>(p, xs, xss, nb, sb, c0, acc);
+        gemv::superblock_dot<B, CPL, false>(p, xv, sb, c0, acc);
       }
       // release the stage once every lane of the warp has read it
       __syncwarp();

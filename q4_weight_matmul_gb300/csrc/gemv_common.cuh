@@ -3,17 +3,34 @@
 // lane's share of a Q4_K superblock with them (genie-ai-runtime §4, Path C:
 // quants read as whole words and dequantised in registers).
 //
-// Activations.  Each 32-wide sub-block j of x is held as a 23-bit fixed-point
-// integer X = rint(x / s_j) with a power-of-two scale s_j = 2^(e-22), e the
-// exponent of the sub-block's largest |x| (so |X| <= 2^22 and
-// |x - s_j*X| <= s_j/2 <= 2^-22 * max|x|), split into three byte planes
-// X = 65536*X2 + 256*X1 + X0 (X0, X1 unsigned, X2 signed).  The 4-bit quants
-// q enter dp4a dot products with the planes unchanged, so P_j = sum q*X over
-// the sub-block is an exact integer; the per-sub-block scales are applied in
-// fp32 registers:
-//     acc += d*sc_j*s_j*P_j - dmin*m_j*XS_j,    XS_j = sum of x over j.
+// Activations.  Each 32-wide sub-block j of x is held as a 32-bit fixed-point
+// integer X = rint(x / s_j) with a power-of-two scale s_j = 2^(e-30), e the
+// exponent of the sub-block's largest |x| (so |X| <= 2^30), written in four
+// balanced base-256 digits X = 2^24*D3 + 2^16*D2 + 2^8*D1 + D0, every digit a
+// signed byte in [-128, 127].  The 4-bit quants q enter dp4a dot products with
+// the digit planes unchanged, so each plane sum sum(q*D) is an exact integer
+// of magnitude <= 15*128*32, and so is every pair 256*P_hi + P_lo of them; a
+// sub-block's value is then formed as
+//     tier 1:  P/256 ~ fmaf(256*P3 + P2, 256, P1)            (D0 dropped)
+//     tier 2:  the same, plus P0/256 added as a second term
+// and the scales are applied in fp32 registers:
+//     acc += d*sc_j*s'_j*V_j - dmin*m_j*XS_j,   s'_j = 256*s_j, XS_j = sum x.
+// Balanced digits keep every plane sum within twice sum q|X|, so combining
+// the planes never cancels more than that.
+//
+// Tiers (chosen per sub-block when x is staged; all lanes of a warp read the
+// same activations, so a tier is a warp-uniform branch):
+//  - tier 1 (three planes D3..D1): every element keeps |x - s'*X'| <= 2^-14 |x|;
+//  - tier 2 (all four planes): some element would not, but every nonzero
+//    element keeps |x - s*X| <= 2^-14 |x| (a wide range inside the block);
+//  - tier 3 (fp32): any other block -- an element below ~2^-16 of the
+//    block's largest, or a largest |x| outside [2^-87, 2^94) -- is staged
+//    with scale 0 (and its fp32 activations in a small pool) and takes
+//    V_j = sum q*x by fp32 multiply-adds after the integer loop.
 // A 32-bit word of quants (8 weights) costs a shift, two LOP3s and six dp4a
-// per token, against one fp32 multiply-add per weight for a dequantised dot.
+// per token (tier 2 adds a pass of one dp4a per 4 weights over its
+// sub-blocks), against one fp32 multiply-add per weight for a dequantised
+// dot.
 #pragma once
 
 #include "q4k_internal.h"
@@ -25,14 +42,14 @@
 namespace q4k {
 namespace gemv {
 
-constexpr int kRegion = 208;   // bytes per (token, superblock, chunk) of x planes: 192 + pad
+constexpr int kRegion = 208;   // bytes per (token, superblock, chunk) of the planes D3..D1: 192 + pad
+constexpr int kPoolMax = 256;  // D0 planes of tier-2 sub-blocks a CTA holds (32 bytes each)
+constexpr int kPool3Max = 32;  // fp32 activations of tier-3 sub-blocks a CTA holds (128 bytes each)
+constexpr uint32_t kNoSlot = 0x3FFFu;   // a tier-3 sub-block without a pool slot reads x from global memory
+// biased fp32 exponents of a sub-block's largest |x| staged in fixed point
+constexpr int kEFixedMin = 40;    // 2^-87
+constexpr int kEFixedMax = 220;   // below 2^94
 
-// acc += dot of the four unsigned bytes of a and of b
-__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int acc) {
-  int d;
-  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(acc));
-  return d;
-}
 // acc += dot of the four unsigned bytes of a and the four signed bytes of b
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int acc) {
   int d;
@@ -61,23 +78,98 @@ __device__ __noinline__ inline bool wait_issued(volatile int* issued, int j) {
   return true;
 }
 
-// Shared-memory bytes of the staged activations: planes, then (scale, sum)
-// pairs per sub-block.
+// Shared-memory bytes of the staged activations: the planes D3..D1 (xs),
+// then (xss) the pool counters, the (scale, sum) pair and the tag of every
+// sub-block, the pool of D0 planes and the pool of tier-3 activations.  Only the counters sit at a fixed
+// offset; the rest is laid out for the nb being staged.
+__host__ __device__ constexpr int pool_entries(int B, int nb) { return B * nb * 8 < kPoolMax ? B * nb * 8 : kPoolMax; }
+__host__ __device__ constexpr int pool3_entries(int B, int nb) { return B * nb * 8 < kPool3Max ? B * nb * 8 : kPool3Max; }
+__host__ __device__ constexpr size_t ss_offset() { return 16; }
+__host__ __device__ constexpr size_t tag_offset(int B, int nb) { return 16 + sizeof(float2) * (size_t)B * nb * 8; }
+__host__ __device__ constexpr size_t pool_offset(int B, int nb) {
+  return (tag_offset(B, nb) + sizeof(uint16_t) * (size_t)B * nb * 8 + 15) & ~size_t(15);
+}
 __host__ __device__ constexpr size_t xs_bytes(int B, int nb) { return (size_t)B * nb * 4 * kRegion; }
-__host__ __device__ constexpr size_t xss_bytes(int B, int nb) { return sizeof(float2) * (size_t)B * nb * 8; }
+__host__ __device__ constexpr size_t pool3_offset(int B, int nb) {
+  return pool_offset(B, nb) + 32 * (size_t)pool_entries(B, nb);
+}
+__host__ __device__ constexpr size_t xss_bytes(int B, int nb) {
+  return pool3_offset(B, nb) + 128 * (size_t)pool3_entries(B, nb);
+}
 
-// Stage x [B][nb*256] once per CTA as byte planes of 23-bit fixed point, with
-// each sub-block's scale s_j and fp32 sum XS_j.  Eight lanes hold one
-// sub-block (four elements each), so its max and sum are three shuffles; all
-// loads of a round are issued before any use.  NT threads (a multiple of 32,
-// tid < NT) take part.  kCoherent reads x through L2 only (x may have been
-// written earlier in the same kernel); otherwise through the read-only path.
+// Staged activations as the consumers read them.
+struct XView {
+  const uint8_t* planes;   // [B][nb][4 chunks][kRegion]: planes D3..D1
+  const float2* ss;        // [B][nb][8]: (scale s', fp32 sum of x); s' = 0 in tier 3
+  const uint16_t* tag;     // [B][nb][8]: bits 0-1 tier-1 (0), -2 (1) or -3 (2); bits 2.. pool slot
+  const uint8_t* pool;     // [slot][32]: the D0 plane of a tier-2 sub-block
+  const float* pool3;      // [slot][32]: the activations of a tier-3 sub-block
+  const float* x;          // the activations themselves, [B][nb*256] (tier 3)
+  int nb;
+};
+
+struct XSmem {
+  uint16_t* tag;
+  uint8_t* pool;
+  int* count;
+};
+
+__device__ __forceinline__ XView make_view(const uint8_t* xs, const float2* xss, const float* x, int B, int nb) {
+  const uint8_t* base = reinterpret_cast<const uint8_t*>(xss);
+  XView v;
+  v.planes = xs;
+  v.ss = reinterpret_cast<const float2*>(base + ss_offset());
+  v.tag = reinterpret_cast<const uint16_t*>(base + tag_offset(B, nb));
+  v.pool = base + pool_offset(B, nb);
+  v.pool3 = reinterpret_cast<const float*>(base + pool3_offset(B, nb));
+  v.x = x;
+  v.nb = nb;
+  return v;
+}
+
+// The pool counters that stage_x allocates slots from: counter[gen & 1] for
+// the D0 pool and counter[2 + (gen & 1)] for the tier-3 pool in staging
+// number `gen`; stage_x zeroes the other two for the next staging.  Zero all
+// four before the first stage_x.
+__device__ __forceinline__ int* pool_counter(float2* xss) { return reinterpret_cast<int*>(xss); }
+
+// byte k (0..3) of each of four words, gathered into one word
+__device__ __forceinline__ uint32_t gather_byte(uint32_t a, uint32_t b, uint32_t c, uint32_t d, int k) {
+  const uint32_t sel = (uint32_t)k | ((uint32_t)(k + 4) << 4);
+  return __byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410);
+}
+
+// Stage x [B][nb*256] once per CTA as balanced-digit planes of 32-bit fixed
+// point, with each sub-block's scale, fp32 sum and tier.  Eight lanes hold
+// one sub-block (four elements each), so its max and sum are three shuffles
+// and its tier one ballot; all loads of a round are issued before any use.
+// NT threads (a multiple of 32, tid < NT) take part; `gen` numbers the
+// stagings of one CTA (0, 1, 2, ...), and the pool counter of this one
+// (pool_counter) must be zero when they enter.  kCoherent reads x through L2 only (x may have
+// been written earlier in the same kernel); otherwise through the read-only
+// path.
 // Plane layout per (token, superblock, chunk c): 16-byte words at
-// ((h*3 + p)*2 + s)*16, h = half of the chunk's 32 positions, p = plane,
-// s = sub-block 2c (0) or 2c+1 (1); word k of it holds positions 16h+4k..+3.
+// ((h*3 + p)*2 + s)*16, h = half of the chunk's 32 positions, p = plane
+// (0, 1, 2 = digits D1, D2, D3), s = sub-block 2c (0) or 2c+1 (1); word k of
+// it holds positions 16h+4k..+3.  A tier-2 sub-block's D0 plane takes a
+// pool slot of 32 bytes (word k: positions 4k..4k+3); when the pool is full
+// the sub-block goes to tier 3 instead.
 template <int B, int NT, bool kCoherent>
 __device__ __forceinline__ void stage_x(const float* __restrict__ x, int nb, uint8_t* xs, float2* xss,
-                                        int tid) {
+                                        int tid, int gen) {
+  uint8_t* xb = reinterpret_cast<uint8_t*>(xss);
+  float2* ssv = reinterpret_cast<float2*>(xb + ss_offset());
+  uint16_t* tag = reinterpret_cast<uint16_t*>(xb + tag_offset(B, nb));
+  uint32_t* pool = reinterpret_cast<uint32_t*>(xb + pool_offset(B, nb));
+  float* pool3 = reinterpret_cast<float*>(xb + pool3_offset(B, nb));
+  int* pool_count = pool_counter(xss) + (gen & 1);
+  int* pool3_count = pool_counter(xss) + 2 + (gen & 1);
+  if (tid == 0) {
+    pool_counter(xss)[(gen + 1) & 1] = 0;
+    pool_counter(xss)[2 + ((gen + 1) & 1)] = 0;
+  }
+  const int pool_cap = pool_entries(B, nb), pool3_cap = pool3_entries(B, nb);
+  const int lane = tid & 31;
   const int row4 = nb * 64;                     // float4 per activation row
   const int n4 = B * row4;                      // a multiple of 64: whole warps
   const float4* x4 = reinterpret_cast<const float4*>(x);
@@ -103,36 +195,136 @@ __device__ __forceinline__ void stage_x(const float* __restrict__ x, int nb, uin
           sum += __shfl_xor_sync(0xffffffffu, sum, o);
         }
         // power-of-two scale: |x| < 2^(E-126) for the biased exponent E of
-        // amax, so X = rint(x * 2^(148-E)) satisfies |X| <= 2^22; blocks
-        // below 2^-104 (and all-zero blocks) are staged as zero
+        // amax, so X = rint(x * 2^(156-E)) satisfies |X| <= 2^30
         const int E = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
-        const bool live = E >= 22;
-        const float mul = live ? __uint_as_float((uint32_t)(275 - E) << 23) : 0.0f;
-        const float scale = live ? __uint_as_float((uint32_t)(E - 21) << 23) : 0.0f;
-        const int X0 = __float2int_rn(v[u].x * mul), X1 = __float2int_rn(v[u].y * mul);
-        const int X2 = __float2int_rn(v[u].z * mul), X3 = __float2int_rn(v[u].w * mul);
+        const bool fixed = E >= kEFixedMin && E <= kEFixedMax;
+        const float mul = fixed ? __uint_as_float((uint32_t)(283 - E) << 23) : 0.0f;
+        const float s24 = fixed ? __uint_as_float((uint32_t)(E - 21) << 23) : 0.0f;   // 2^(E-148)
+        const float xv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t dg[4];
+        bool t2 = false, t3 = false;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int X = __float2int_rn(xv[i] * mul);
+          // balanced base-256 digits, each as a signed byte
+          dg[i] = ((uint32_t)X + 0x80808080u) ^ 0x80808080u;
+          const int ax = abs(X), d0 = abs((int)(int8_t)(dg[i] & 0xFFu));
+          const bool nz = xv[i] != 0.0f;
+          const bool e3 = nz && (!fixed || ax < (1 << 13));
+          t3 = t3 || e3;
+          t2 = t2 || e3 || (nz && ((d0 + 1) << 14) > ax);
+        }
         uint32_t* dst = reinterpret_cast<uint32_t*>(xs + (((size_t)b * nb + sb) * 4 + c) * kRegion) +
                         (h * 3 * 2 + sf) * 4 + kw;
 #pragma unroll
-        for (int pl = 0; pl < 3; ++pl) {
-          const int sh = 8 * pl;
-          const uint32_t word = ((uint32_t)(X0 >> sh) & 0xFFu) | (((uint32_t)(X1 >> sh) & 0xFFu) << 8) |
-                                (((uint32_t)(X2 >> sh) & 0xFFu) << 16) | (((uint32_t)(X3 >> sh) & 0xFFu) << 24);
-          dst[pl * 2 * 4] = word;
+        for (int pl = 0; pl < 3; ++pl) dst[pl * 2 * 4] = gather_byte(dg[0], dg[1], dg[2], dg[3], pl + 1);
+        // a sub-block's tier: any of its eight lanes; tier 2 takes a pool slot
+        const unsigned b2 = __ballot_sync(0xffffffffu, t2), b3 = __ballot_sync(0xffffffffu, t3);
+        const int grp = lane & 24;
+        const bool g2 = ((b2 >> grp) & 0xFFu) != 0;
+        bool g3 = ((b3 >> grp) & 0xFFu) != 0;
+        int slot = 0;
+        if ((idx & 7) == 0 && g2 && !g3) slot = atomicAdd(pool_count, 1);
+        slot = __shfl_sync(0xffffffffu, slot, grp);
+        if (g2 && !g3) {
+          if (slot < pool_cap) pool[(size_t)slot * 8 + (pos >> 2)] = gather_byte(dg[0], dg[1], dg[2], dg[3], 0);
+          else g3 = true;
         }
-        if ((idx & 7) == 0) xss[((size_t)b * nb + sb) * 8 + j] = make_float2(scale, sum);
+        // a tier-3 sub-block keeps its fp32 activations in the pool if it can
+        int slot3 = 0;
+        if ((idx & 7) == 0 && g3) slot3 = atomicAdd(pool3_count, 1);
+        slot3 = __shfl_sync(0xffffffffu, slot3, grp);
+        if (g3 && slot3 < pool3_cap) reinterpret_cast<float4*>(pool3 + (size_t)slot3 * 32)[pos >> 2] = v[u];
+        if ((idx & 7) == 0) {
+          const size_t e = ((size_t)b * nb + sb) * 8 + j;
+          ssv[e] = make_float2(g3 ? 0.0f : s24, sum);
+          const uint32_t s3 = slot3 < pool3_cap ? (uint32_t)slot3 : kNoSlot;
+          tag[e] = (uint16_t)(g3 ? 2u | (s3 << 2) : (g2 ? 1u | ((uint32_t)slot << 2) : 0u));
+        }
       }
     }
   }
 }
 
+// fp32 dot of the 32 quants of sub-block j of the BLOCK144 superblock at
+// `p` (shared memory) with its activations (the tier-3 path): xs[0..31] in
+// shared memory, or, without a pool slot, xg[0..31] in global memory
+template <bool kCoherent>
+__device__ __forceinline__ float subblock_fp32(const uint8_t* p, int j, const float* xs, const float* xg) {
+  const uint8_t* qs = p + 16 + 32 * (j >> 1);
+  const int sh = (j & 1) ? 4 : 0;
+  float v = 0.0f;
+  if (xs) {
+#pragma unroll 8
+    for (int l = 0; l < 32; ++l) v = fmaf((float)((qs[l] >> sh) & 15), xs[l], v);
+  } else {
+#pragma unroll 8
+    for (int l = 0; l < 32; ++l) {
+      const float xl = kCoherent ? __ldcg(xg + l) : __ldg(xg + l);
+      v = fmaf((float)((qs[l] >> sh) & 15), xl, v);
+    }
+  }
+  return v;
+}
+
+// Tier-2 correction of sub-block j of the BLOCK144 superblock at `p`: the
+// exact integer sum of q * D0 (the fourth digit plane, a 32-byte pool entry)
+// over its 32 weights.
+__device__ __forceinline__ int subblock_plane0(const uint8_t* p, int j, const uint8_t* d0) {
+  const uint8_t* qs = p + 16 + 32 * (j >> 1);
+  const int hi = j & 1;
+  int acc = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4 qq = *reinterpret_cast<const uint4*>(qs + 16 * h);
+    const uint4 xw = reinterpret_cast<const uint4*>(d0)[h];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w = word_of(qq, k);
+      acc = dp4a_us(hi ? (w >> 4) & 0x0F0F0F0Fu : w & 0x0F0F0F0Fu, word_of(xw, k), acc);
+    }
+  }
+  return acc;
+}
+
+// What tier-2 and tier-3 sub-blocks among chunks c0 .. c0+cpl-1 add to the
+// lane's scaled sum for token b: sc_j s'_j (sum q*D0) / 256 for tier 2;
+// sc_j sum q*x in fp32, straight from x, for tier 3 (staged with scale 0, so
+// the planes added nothing).  Out of line: the main loop keeps its registers.
+template <bool kCoherent>
+__device__ __noinline__ float tier_fix(const uint8_t* p, const XView X, int sb, int c0, int cpl, int b,
+                                       uint32_t sc03, uint32_t sc47) {
+  const int nb = X.nb;
+  const uint16_t* tg = X.tag + ((size_t)b * nb + sb) * 8;
+  const float2* ssb = X.ss + ((size_t)b * nb + sb) * 8;
+  float add = 0.0f;
+  for (int j = 2 * c0; j < 2 * (c0 + cpl); ++j) {
+    const uint32_t t = tg[j];
+    if (!(t & 3u)) continue;
+    const float sc = byte_f(j < 4 ? sc03 : sc47, j & 3);
+    if (t & 2u) {
+      const float* xg = X.x + (size_t)b * nb * 256 + (size_t)sb * 256 + 32 * j;
+      const float* xs = (t >> 2) != kNoSlot ? X.pool3 + 32 * (size_t)(t >> 2) : nullptr;
+      add = fmaf(sc, subblock_fp32<kCoherent>(p, j, xs, xg), add);
+    } else {
+      add = fmaf(sc * ssb[j].x, (float)subblock_plane0(p, j, X.pool + 32 * (size_t)(t >> 2)) * 0.00390625f, add);
+    }
+  }
+  return add;
+}
+
 // One lane's share of one superblock row against the staged activations:
 // chunks c0 .. c0+CPL-1 (64 weights each) of the BLOCK144 superblock at `p`
 // (shared memory), superblock index sb of x.  acc[b] receives
-// d * sum_j sc_j s_j P_j - dmin * sum_j m_j XS_j over the lane's sub-blocks.
-template <int B, int CPL>
-__device__ __forceinline__ void superblock_dot(const uint8_t* p, const uint8_t* xs, const float2* xss, int nb,
-                                               int sb, int c0, float (&acc)[B]) {
+// d * sum_j sc_j s'_j V_j - dmin * sum_j m_j XS_j over the lane's sub-blocks.
+// The main loop takes the three planes D3..D1 of every sub-block, with no
+// branch; tier-2 and tier-3 sub-blocks are completed after it (tier_fix).
+// With balanced digits every partial value is within twice sum q|X|, so
+// adding the D0 term as a separately rounded term costs at most 2^-22 of that.
+template <int B, int CPL, bool kCoherent>
+__device__ __forceinline__ void superblock_dot(const uint8_t* p, const XView& X, int sb, int c0,
+                                               float (&acc)[B]) {
+  const int nb = X.nb;
   const uint4 hd = *reinterpret_cast<const uint4*>(p);
   const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
   // scales (sc) and mins (m) of sub-blocks 0..3 and 4..7, one byte each
@@ -147,14 +339,14 @@ __device__ __forceinline__ void superblock_dot(const uint8_t* p, const uint8_t* 
     const int c = c0 + cc;
     const uint4 q0 = *reinterpret_cast<const uint4*>(p + 16 + 32 * c);
     const uint4 q1 = *reinterpret_cast<const uint4*>(p + 32 + 32 * c);
-    // exact integer sums of q * X per plane, low (sub-block 2c) and high
-    // (2c+1) nibbles
+    // exact integer sums of q * D per digit plane D1..D3, low (sub-block 2c)
+    // and high (2c+1) nibbles
     int lo[B][3], hi[B][3];
 #pragma unroll
     for (int b = 0; b < B; ++b)
 #pragma unroll
       for (int pl = 0; pl < 3; ++pl) lo[b][pl] = hi[b][pl] = 0;
-    const uint8_t* xc0 = xs + ((size_t)sb * 4 + c) * kRegion;
+    const uint8_t* xc0 = X.planes + ((size_t)sb * 4 + c) * kRegion;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint4 qq = h ? q1 : q0;
@@ -173,13 +365,8 @@ __device__ __forceinline__ void superblock_dot(const uint8_t* p, const uint8_t* 
           const uint4 xl = xp[2 * pl], xh = xp[2 * pl + 1];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            if (pl < 2) {
-              lo[b][pl] = dp4a_uu(ql[k], word_of(xl, k), lo[b][pl]);
-              hi[b][pl] = dp4a_uu(qh[k], word_of(xh, k), hi[b][pl]);
-            } else {
-              lo[b][pl] = dp4a_us(ql[k], word_of(xl, k), lo[b][pl]);
-              hi[b][pl] = dp4a_us(qh[k], word_of(xh, k), hi[b][pl]);
-            }
+            lo[b][pl] = dp4a_us(ql[k], word_of(xl, k), lo[b][pl]);
+            hi[b][pl] = dp4a_us(qh[k], word_of(xh, k), hi[b][pl]);
           }
         }
       }
@@ -191,16 +378,27 @@ __device__ __forceinline__ void superblock_dot(const uint8_t* p, const uint8_t* 
     const float m_lo = byte_f(mw, bi), m_hi = byte_f(mw, bi + 1);
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-      // P = 65536*P2 + (256*P1 + P0); the bracket is an exact int32
-      const float p_lo = fmaf((float)lo[b][2], 65536.0f, (float)(lo[b][1] * 256 + lo[b][0]));
-      const float p_hi = fmaf((float)hi[b][2], 65536.0f, (float)(hi[b][1] * 256 + hi[b][0]));
-      const float4 ss = *reinterpret_cast<const float4*>(xss + ((size_t)b * nb + sb) * 8 + 2 * c);
-      scaled[b] = fmaf(sc_hi * ss.z, p_hi, fmaf(sc_lo * ss.x, p_lo, scaled[b]));
+      // (P - D0 term) / 256 in units of s' = 256 s, one rounding
+      const float v_lo = fmaf((float)(lo[b][2] * 256 + lo[b][1]), 256.0f, (float)lo[b][0]);
+      const float v_hi = fmaf((float)(hi[b][2] * 256 + hi[b][1]), 256.0f, (float)hi[b][0]);
+      const float4 ss = *reinterpret_cast<const float4*>(X.ss + ((size_t)b * nb + sb) * 8 + 2 * c);
+      scaled[b] = fmaf(sc_hi * ss.z, v_hi, fmaf(sc_lo * ss.x, v_lo, scaled[b]));
       mins[b] = fmaf(m_hi, ss.w, fmaf(m_lo, ss.y, mins[b]));
     }
   }
 #pragma unroll
   for (int b = 0; b < B; ++b) acc[b] = fmaf(dm.x, scaled[b], -dm.y * mins[b]);
+  // tier-2 and tier-3 sub-blocks among the lane's chunks
+#pragma unroll
+  for (int b = 0; b < B; ++b) {
+    // the tags of the lane's sub-blocks 2c0 .. 2(c0+CPL)-1, two per word
+    const uint4 t8 = *reinterpret_cast<const uint4*>(X.tag + ((size_t)b * nb + sb) * 8);
+    uint32_t any;
+    if (CPL == 4) any = t8.x | t8.y | t8.z | t8.w;
+    else if (CPL == 2) any = c0 ? (t8.z | t8.w) : (t8.x | t8.y);
+    else any = word_of(t8, c0);
+    if (any & 0x00030003u) acc[b] = fmaf(dm.x, tier_fix<kCoherent>(p, X, sb, c0, CPL, b, sc03, sc47), acc[b]);
+  }
 }
 
 }  // namespace gemv

@@ -42,8 +42,8 @@
 // leaves one partial per row in shared memory, and after a pass of units the
 // CTA adds each row's partials in superblock order (deterministic).
 //
-// Arithmetic: 23-bit fixed-point activation planes and exact integer dp4a
-// block sums, scales applied in fp32 (gemv_common.cuh).
+// Arithmetic: 32-bit fixed-point activation digit planes and exact integer
+// dp4a block sums, scales applied in fp32 (gemv_common.cuh).
 #include "gemv_common.cuh"
 #include "q4k_internal.h"
 #include "tc_ptx.cuh"
@@ -219,8 +219,8 @@ __device__ __forceinline__ float* piece_of(const SeqParams& P, const SeqEpoch& E
 template <int B>
 __device__ __forceinline__ void consume_pass(const SeqParams& P, const uint8_t* ring_base, uint64_t* full,
                                              uint64_t* empty, volatile int* issued, int ring, int J, int ps,
-                                             int pe, long long u0, int nb, int nu, const uint8_t* xs,
-                                             const float2* xss, float* part, bool& ok, int warp, int lane) {
+                                             int pe, long long u0, int nb, int nu, const gemv::XView& xv,
+                                             float* part, bool& ok, int warp, int lane) {
   for (int s = ps + warp; s < pe; s += kConsumerWarps) {
     const int j = J + s;
     const int slot = j % ring;
@@ -241,10 +241,10 @@ __device__ __forceinline__ void consume_pass(const SeqParams& P, const uint8_t* 
     if (ok) {
       const int sb = (int)((u0 + s) % nu) * kUnitSB;
       const uint8_t* p = ring_base + (size_t)slot * kUnitBytes + lane * kBlockBytes;
-      gemv::superblock_dot<B, 4>(p, xs, xss, nb, sb, 0, acc);
+      gemv::superblock_dot<B, 4, true>(p, xv, sb, 0, acc);
       if (sb + 1 < nb) {
         float acc2[B];
-        gemv::superblock_dot<B, 4>(p + kRB * kBlockBytes, xs, xss, nb, sb + 1, 0, acc2);
+        gemv::superblock_dot<B, 4, true>(p + kRB * kBlockBytes, xv, sb + 1, 0, acc2);
 #pragma unroll
         for (int b = 0; b < B; ++b) acc[b] += acc2[b];
       }
@@ -318,6 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
     }
     *issued = 0;
     flags[0] = flags[1] = flags[2] = 0;
+    int* pc = gemv::pool_counter(xss);
+    pc[0] = pc[1] = pc[2] = pc[3] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -379,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
   const float* staged_x = nullptr;
   int staged_nb = -1;
   int J = 0;          // this CTA's stages so far (ring order)
+  int n_staged = 0;   // activation stagings so far (pool counter generation)
   int pass_no = 0;
   constexpr int per = kRB * B;
   for (int ei = 0; ei < P.n_epoch; ++ei) {
@@ -407,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
       const long long u0 = u - S.unit_base, u1 = (e1 < su1 ? e1 : su1) - S.unit_base;   // segment units
       const int n_units = (int)(u1 - u0);
       if (S.x != staged_x || nb != staged_nb) {
-        gemv::stage_x<B, kConsumers, true>(S.x, nb, xs, xss, tid);
+        gemv::stage_x<B, kConsumers, true>(S.x, nb, xs, xss, tid, n_staged++);
         staged_x = S.x;
         staged_nb = nb;
         named_sync_consumers();
@@ -415,8 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
       const int pu = P.part_floats / per;   // units per pass
       for (int ps = 0; ps < n_units; ps += pu, ++pass_no) {
         const int pe = min(ps + pu, n_units);
-        consume_pass<B>(P, ring_base, full, empty, issued, ring, J, ps, pe, u0, nb, nu, xs, xss, part, ok, warp,
-                        lane);
+        consume_pass<B>(P, ring_base, full, empty, issued, ring, J, ps, pe, u0, nb, nu,
+                        gemv::make_view(xs, xss, S.x, B, nb), part, ok, warp, lane);
         if (!ok) flags[2] = 1;
         named_sync_consumers();
         ok = ok && !flags[2];
@@ -640,9 +643,9 @@ int plan_launch(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& i
   return Q4K_OK;
 }
 
+// Set once per device and batch: the kernel may use the opt-in shared memory.
 template <int B>
-cudaError_t launch_seq_b(const SeqParams& P, const SeqPlan& p, int dev, const DeviceInfo& info,
-                         cudaStream_t s) {
+cudaError_t allow_smem(int dev, const DeviceInfo& info) {
   static int s_limit[64];
   int& limit = s_limit[dev & 63];
   if (limit < info.max_smem_optin) {
@@ -651,6 +654,25 @@ cudaError_t launch_seq_b(const SeqParams& P, const SeqPlan& p, int dev, const De
     if (e != cudaSuccess) return e;
     limit = info.max_smem_optin;
   }
+  return cudaSuccess;
+}
+
+cudaError_t allow_smem_batch(int batch, int dev, const DeviceInfo& info) {
+  switch (batch) {
+    case 1: return allow_smem<1>(dev, info);
+    case 2: return allow_smem<2>(dev, info);
+    case 3: return allow_smem<3>(dev, info);
+    case 4: return allow_smem<4>(dev, info);
+    case 5: return allow_smem<5>(dev, info);
+    case 6: return allow_smem<6>(dev, info);
+    case 7: return allow_smem<7>(dev, info);
+    case 8: return allow_smem<8>(dev, info);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+template <int B>
+cudaError_t launch_seq_b(const SeqParams& P, const SeqPlan& p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid);
   cfg.blockDim = dim3(kThreads);
@@ -665,9 +687,131 @@ cudaError_t launch_seq_b(const SeqParams& P, const SeqPlan& p, int dev, const De
   return cudaLaunchKernelEx(&cfg, gemv_seq_kernel<B>, P);
 }
 
+cudaError_t launch_seq_batch(const SeqParams& P, const SeqPlan& p, int batch, cudaStream_t s) {
+  switch (batch) {
+    case 1: return launch_seq_b<1>(P, p, s);
+    case 2: return launch_seq_b<2>(P, p, s);
+    case 3: return launch_seq_b<3>(P, p, s);
+    case 4: return launch_seq_b<4>(P, p, s);
+    case 5: return launch_seq_b<5>(P, p, s);
+    case 6: return launch_seq_b<6>(P, p, s);
+    case 7: return launch_seq_b<7>(P, p, s);
+    case 8: return launch_seq_b<8>(P, p, s);
+    default: return cudaErrorNotSupported;
+  }
+}
+
 // Launches of a job list: consecutive chunks of at most kLaunchJobs jobs
 // (stream order between launches is a full dependency).
 int next_chunk(int i0, int n_jobs) { return std::min(n_jobs, i0 + kLaunchJobs); }
+int n_launches(int n_jobs) { return n_jobs <= 0 ? 1 : (n_jobs + kLaunchJobs - 1) / kLaunchJobs; }
+
+// A prepared job list in caller-owned host memory: a header, then one
+// (kernel parameters, launch shape) pair per launch.
+constexpr uint64_t kPlanMagic = 0x71346b5365715031ull;   // "q4kSeqP1"
+
+struct SeqLaunch {
+  SeqParams P;       // first: the tensor maps need 64-byte alignment
+  SeqPlan plan;
+  int active;        // 0: the chunk holds no work (every job has 0 rows)
+};
+
+struct alignas(64) PlanHeader {
+  uint64_t magic;
+  int n_launch, batch, dev;
+  size_t ws_need;     // workspace bytes the launches need
+  size_t counters;    // leading workspace bytes that must start at zero
+  const void* ws;     // bound workspace
+};
+
+size_t plan_bytes_for(int n_jobs) {
+  return sizeof(PlanHeader) + sizeof(SeqLaunch) * (size_t)n_launches(n_jobs);
+}
+
+// Plan every launch of a job list into `buf`: segments, epochs, CTA shares,
+// tensor maps, the workspace it needs.  Enqueues nothing.  With `ws` null
+// the workspace is bound later (bind_workspace).
+int build_plan(const q4k_gemv_job* jobs, int n_jobs, int batch, void* buf, size_t bytes, cudaError_t* ce) {
+  *ce = cudaSuccess;
+  if (bytes < plan_bytes_for(n_jobs)) return Q4K_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(buf) & 63u) != 0) return Q4K_ERR_ALIGNMENT;
+  int dev = 0;
+  if ((*ce = cudaGetDevice(&dev)) != cudaSuccess) return Q4K_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return Q4K_ERR_UNSUPPORTED;
+  const DeviceInfo& info = device_info(dev);
+  int* err = device_error_word();
+  if (!err) {
+    *ce = cudaGetLastError();
+    return Q4K_ERR_CUDA;
+  }
+  PlanHeader* h = static_cast<PlanHeader*>(buf);
+  SeqLaunch* L = reinterpret_cast<SeqLaunch*>(static_cast<uint8_t*>(buf) + sizeof(PlanHeader));
+  h->magic = 0;
+  size_t need = kSyncBytes;
+  int k = 0;
+  for (int i0 = 0; i0 < n_jobs || k == 0; i0 = next_chunk(i0, n_jobs), ++k) {
+    SeqLaunch& l = L[k];
+    std::memset(&l.P, 0, sizeof(l.P));
+    const int st = plan_launch(jobs + i0, next_chunk(i0, n_jobs) - i0, batch, info, &l.P, &l.plan);
+    if (st == Q4K_ERR_CUDA) *ce = cudaErrorInvalidValue;   // a tensor map the driver refused
+    if (st != Q4K_OK) return st;
+    l.active = l.plan.n_epoch > 0;
+    l.P.err = err;
+    need = std::max(need, l.plan.ws_bytes);
+    if (n_jobs == 0) {
+      ++k;
+      break;
+    }
+  }
+  if ((*ce = allow_smem_batch(batch, dev, info)) != cudaSuccess) return Q4K_ERR_CUDA;
+  h->n_launch = k;
+  h->batch = batch;
+  h->dev = dev;
+  h->ws_need = need;
+  h->counters = kSyncBytes + (((sizeof(unsigned) * 2 * (size_t)info.sm_count) + 255) & ~size_t(255));
+  h->ws = nullptr;
+  h->magic = kPlanMagic;
+  return Q4K_OK;
+}
+
+int bind_workspace(void* buf, void* ws, size_t ws_bytes) {
+  PlanHeader* h = static_cast<PlanHeader*>(buf);
+  if (ws_bytes < h->ws_need) return Q4K_ERR_INVALID_ARG;
+  SeqLaunch* L = reinterpret_cast<SeqLaunch*>(static_cast<uint8_t*>(buf) + sizeof(PlanHeader));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  for (int k = 0; k < h->n_launch; ++k) {
+    L[k].P.sync = reinterpret_cast<unsigned*>(w);
+    L[k].P.tickets = reinterpret_cast<unsigned*>(w + L[k].plan.tickets_off);
+    L[k].P.pieces = reinterpret_cast<float*>(w + L[k].plan.pieces_off);
+  }
+  h->ws = ws;
+  return Q4K_OK;
+}
+
+int run_plan(const void* buf, cudaStream_t s, cudaError_t* ce) {
+  *ce = cudaSuccess;
+  const PlanHeader* h = static_cast<const PlanHeader*>(buf);
+  if (h->magic != kPlanMagic || !h->ws) return Q4K_ERR_INVALID_ARG;
+  int dev = 0;
+  if ((*ce = cudaGetDevice(&dev)) != cudaSuccess) return Q4K_ERR_CUDA;
+  if (dev != h->dev) return Q4K_ERR_INVALID_ARG;
+  const SeqLaunch* L = reinterpret_cast<const SeqLaunch*>(static_cast<const uint8_t*>(buf) + sizeof(PlanHeader));
+  for (int k = 0; k < h->n_launch; ++k) {
+    if (!L[k].active) continue;
+    if ((*ce = launch_seq_batch(L[k].P, L[k].plan, h->batch, s)) != cudaSuccess) return Q4K_ERR_CUDA;
+  }
+  return Q4K_OK;
+}
+
+// Per-thread plan buffer of the one-shot entry points (a job list of the
+// maximum length takes three launches).
+struct alignas(64) OneShotPlan {
+  uint8_t bytes[sizeof(PlanHeader) + sizeof(SeqLaunch) * ((kGemvSeqMaxJobs + kLaunchJobs - 1) / kLaunchJobs)];
+};
+OneShotPlan* one_shot_plan() {
+  static thread_local OneShotPlan* p = new OneShotPlan;
+  return p;
+}
 
 }  // namespace
 
@@ -686,57 +830,44 @@ int gemv_seq_workspace(const q4k_gemv_job* jobs, int n_jobs, int batch, size_t* 
   return Q4K_OK;
 }
 
+size_t gemv_seq_plan_bytes(int n_jobs) { return plan_bytes_for(n_jobs); }
+
+int gemv_seq_plan(const q4k_gemv_job* jobs, int n_jobs, int batch, void* workspace, size_t workspace_bytes,
+                  void* plan, size_t plan_bytes, cudaError_t* cuda_err) {
+  if (batch == 0 || !workspace) {
+    // nothing to launch (the caller checked that no job has work)
+    *cuda_err = cudaSuccess;
+    if (plan_bytes < sizeof(PlanHeader)) return Q4K_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(plan) & 63u) != 0) return Q4K_ERR_ALIGNMENT;
+    PlanHeader* h = static_cast<PlanHeader*>(plan);
+    int dev = 0;
+    if ((*cuda_err = cudaGetDevice(&dev)) != cudaSuccess) return Q4K_ERR_CUDA;
+    h->n_launch = 0;
+    h->batch = batch;
+    h->dev = dev;
+    h->ws_need = h->counters = 0;
+    h->ws = plan;
+    h->magic = kPlanMagic;
+    return Q4K_OK;
+  }
+  const int st = build_plan(jobs, n_jobs, batch, plan, plan_bytes, cuda_err);
+  if (st != Q4K_OK) return st;
+  const int b = bind_workspace(plan, workspace, workspace_bytes);
+  if (b != Q4K_OK) static_cast<PlanHeader*>(plan)->magic = 0;
+  return b;
+}
+
+int gemv_seq_launch(const void* plan, cudaStream_t s, cudaError_t* cuda_err) { return run_plan(plan, s, cuda_err); }
+
 int launch_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int batch, void* workspace, size_t workspace_bytes,
                     cudaStream_t s, cudaError_t* cuda_err) {
-  *cuda_err = cudaSuccess;
-  int dev = 0;
-  if ((*cuda_err = cudaGetDevice(&dev)) != cudaSuccess) return Q4K_ERR_CUDA;
-  const DeviceInfo& info = device_info(dev);
-  int* err = device_error_word();
-  if (!err) {
-    *cuda_err = cudaGetLastError();
-    return Q4K_ERR_CUDA;
-  }
   // plan every launch before enqueuing any, so that a refused request
   // enqueues nothing
-  size_t need = kSyncBytes;
-  for (int i0 = 0; i0 < n_jobs; i0 = next_chunk(i0, n_jobs)) {
-    SeqPlan p;
-    const int st = plan_launch(jobs + i0, next_chunk(i0, n_jobs) - i0, batch, info, nullptr, &p);
-    if (st != Q4K_OK) return st;
-    need = std::max(need, p.ws_bytes);
-  }
-  if (workspace_bytes < need) return Q4K_ERR_INVALID_ARG;
-  static thread_local SeqParams P;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  for (int i0 = 0; i0 < n_jobs; i0 = next_chunk(i0, n_jobs)) {
-    std::memset(&P, 0, sizeof(P));
-    SeqPlan p;
-    const int st = plan_launch(jobs + i0, next_chunk(i0, n_jobs) - i0, batch, info, &P, &p);
-    if (st != Q4K_OK) return st;
-    if (p.n_epoch == 0) continue;
-    P.sync = reinterpret_cast<unsigned*>(ws);
-    P.tickets = reinterpret_cast<unsigned*>(ws + p.tickets_off);
-    P.pieces = reinterpret_cast<float*>(ws + p.pieces_off);
-    P.err = err;
-    cudaError_t e;
-    switch (batch) {
-      case 1: e = launch_seq_b<1>(P, p, dev, info, s); break;
-      case 2: e = launch_seq_b<2>(P, p, dev, info, s); break;
-      case 3: e = launch_seq_b<3>(P, p, dev, info, s); break;
-      case 4: e = launch_seq_b<4>(P, p, dev, info, s); break;
-      case 5: e = launch_seq_b<5>(P, p, dev, info, s); break;
-      case 6: e = launch_seq_b<6>(P, p, dev, info, s); break;
-      case 7: e = launch_seq_b<7>(P, p, dev, info, s); break;
-      case 8: e = launch_seq_b<8>(P, p, dev, info, s); break;
-      default: return Q4K_ERR_UNSUPPORTED;
-    }
-    if (e != cudaSuccess) {
-      *cuda_err = e;
-      return Q4K_ERR_CUDA;
-    }
-  }
-  return Q4K_OK;
+  OneShotPlan* buf = one_shot_plan();
+  const int st = gemv_seq_plan(jobs, n_jobs, batch, workspace, workspace_bytes, buf->bytes, sizeof(buf->bytes),
+                               cuda_err);
+  if (st != Q4K_OK) return st;
+  return run_plan(buf->bytes, s, cuda_err);
 }
 
 // ---------------------------------------------------------------------------
@@ -774,15 +905,18 @@ int launch_gemv_seq_static(const q4k_gemv_job* jobs, int n_jobs, int batch, cuda
     }
     scratch = g_static_ptr[dev];
   }
-  size_t need = 0;
-  const int st = gemv_seq_workspace(jobs, n_jobs, batch, &need);
+  // plan (and refuse) everything before anything is enqueued
+  OneShotPlan* buf = one_shot_plan();
+  const int st = build_plan(jobs, n_jobs, batch, buf->bytes, sizeof(buf->bytes), cuda_err);
   if (st != Q4K_OK) return st;
-  if (need > kStaticScratchBytes) return Q4K_ERR_UNSUPPORTED;
+  const PlanHeader* h = reinterpret_cast<const PlanHeader*>(buf->bytes);
+  if (h->ws_need > kStaticScratchBytes) return Q4K_ERR_UNSUPPORTED;
+  const int b = bind_workspace(buf->bytes, scratch, kStaticScratchBytes);
+  if (b != Q4K_OK) return b;
   // the arrival counters and tickets must start at zero; a launch that runs
   // to its end leaves them so, and this also covers one that never did
-  const size_t counters = kSyncBytes + (((sizeof(unsigned) * 2 * (size_t)device_info(dev).sm_count) + 255) & ~size_t(255));
-  if ((*cuda_err = cudaMemsetAsync(scratch, 0, counters, s)) != cudaSuccess) return Q4K_ERR_CUDA;
-  return launch_gemv_seq(jobs, n_jobs, batch, scratch, kStaticScratchBytes, s, cuda_err);
+  if ((*cuda_err = cudaMemsetAsync(scratch, 0, h->counters, s)) != cudaSuccess) return Q4K_ERR_CUDA;
+  return run_plan(buf->bytes, s, cuda_err);
 }
 
 }  // namespace q4k

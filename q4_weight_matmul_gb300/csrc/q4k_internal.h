@@ -30,6 +30,9 @@ cudaError_t launch_pack_block144(const uint16_t* d, const uint16_t* dmin,
                                  const uint8_t* q, int64_t rows, int64_t cols,
                                  uint8_t* w, cudaStream_t s);
 
+cudaError_t launch_unpack_block144(const uint8_t* w, int64_t rows, int64_t cols, uint16_t* d, uint16_t* dmin,
+                                   uint8_t* sc, uint8_t* m, uint8_t* q, cudaStream_t s);
+
 cudaError_t launch_q8_quantize(const float* x, int64_t tokens, int64_t cols,
                                int8_t* q, float* d8, int32_t* sum,
                                cudaStream_t s);
@@ -50,6 +53,12 @@ constexpr int kGemvSeqMaxJobs = 256;
 int gemv_seq_workspace(const q4k_gemv_job* jobs, int n_jobs, int batch, size_t* bytes);
 int launch_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int batch, void* workspace, size_t workspace_bytes,
                     cudaStream_t s, cudaError_t* cuda_err);
+// Prepared job lists: the host plan (tensor maps, launch shapes, bound
+// workspace) built once and launched many times.
+size_t gemv_seq_plan_bytes(int n_jobs);
+int gemv_seq_plan(const q4k_gemv_job* jobs, int n_jobs, int batch, void* workspace, size_t workspace_bytes,
+                  void* plan, size_t plan_bytes, cudaError_t* cuda_err);
+int gemv_seq_launch(const void* plan, cudaStream_t s, cudaError_t* cuda_err);
 // The same with the library's built-in scratch array as the workspace.
 int launch_gemv_seq_static(const q4k_gemv_job* jobs, int n_jobs, int batch, cudaStream_t s,
                            cudaError_t* cuda_err);

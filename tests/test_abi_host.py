@@ -52,6 +52,64 @@ def test_packed_bytes(lib):
     assert lib.q4k_packed_bytes(-1, 256, 0) == 0
 
 
+def test_gpu_layout_is_declared_and_refused(lib):
+    assert lib.q4k_packed_bytes(8, 256, 1) == 0                     # Q4K_LAYOUT_GPU
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.q4k_pack(fake, fake, fake, fake, fake, 8, 256, 1, fake, None) == 3
+    assert lib.q4k_unpack(fake, 1, 8, 256, fake, fake, fake, fake, fake, None) == 3
+    assert lib.q4k_gemv(fake, 1, 8, 256, fake, 1, None, fake, None) == 3
+    assert lib.q4k_gemm(fake, 1, 8, 256, fake, fake, fake, 16, fake, None) == 3
+
+
+def test_q8_1_bytes(lib):
+    # q: one byte per element; d8 and sum: four bytes each per 32 elements
+    assert lib.q8_1_bytes(512, 2560) == 512 * 2560 + 2 * 4 * 512 * 80
+    assert lib.q8_1_bytes(1, 256) == 256 + 64
+    assert lib.q8_1_bytes(0, 256) == 0
+    assert lib.q8_1_bytes(4, 100) == 0
+    assert lib.q8_1_bytes(-1, 256) == 0
+
+
+def test_unpack_validates_before_any_launch(lib):
+    fake, odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10004)
+    assert lib.q4k_unpack(fake, 0, 8, 300, fake, fake, fake, fake, fake, None) == 1
+    assert lib.q4k_unpack(fake, 0, -1, 256, fake, fake, fake, fake, fake, None) == 1
+    assert lib.q4k_unpack(None, 0, 8, 256, fake, fake, fake, fake, fake, None) == 1
+    assert lib.q4k_unpack(fake, 0, 8, 256, fake, fake, fake, fake, None, None) == 1
+    assert lib.q4k_unpack(odd, 0, 8, 256, fake, fake, fake, fake, fake, None) == 2
+    assert lib.q4k_unpack(fake, 0, 0, 256, None, None, None, None, None, None) == 0
+
+
+def test_gemv_seq_plan_validates_like_the_one_shot_call(lib):
+    import q4_weight_matmul_gb300 as q4k
+    fake, odd = 0x10000, 0x10004
+
+    def jobs(*specs):
+        arr = (q4k.GemvJob * len(specs))()
+        for i, (rows, cols, x) in enumerate(specs):
+            arr[i].w, arr[i].rows, arr[i].cols, arr[i].x, arr[i].y = fake, rows, cols, x, fake
+        return arr
+
+    n1 = lib.q4k_gemv_seq_plan_bytes(1)
+    assert n1 > 0 and lib.q4k_gemv_seq_plan_bytes(96) == n1              # one launch holds 96 jobs
+    assert lib.q4k_gemv_seq_plan_bytes(97) > n1
+    assert lib.q4k_gemv_seq_plan_bytes(256) > lib.q4k_gemv_seq_plan_bytes(97)
+    assert lib.q4k_gemv_seq_plan_bytes(257) == 0 and lib.q4k_gemv_seq_plan_bytes(-1) == 0
+    raw = ctypes.create_string_buffer(n1 + 128)
+    base = ctypes.addressof(raw)
+    plan = base + (-base) % 64
+    ws = ctypes.c_void_p(fake)
+    ok1 = jobs((8, 256, fake))
+    assert lib.q4k_gemv_seq_plan(None, 1, 0, 1, ws, 1 << 20, plan, n1) == 1          # null list
+    assert lib.q4k_gemv_seq_plan(ok1, 1, 5, 1, ws, 1 << 20, plan, n1) == 3            # unknown layout
+    assert lib.q4k_gemv_seq_plan(ok1, 1, 0, 9, ws, 1 << 20, plan, n1) == 3            # batch above 8
+    assert lib.q4k_gemv_seq_plan(jobs((8, 300, fake)), 1, 0, 1, ws, 1 << 20, plan, n1) == 1
+    assert lib.q4k_gemv_seq_plan(jobs((8, 256, odd)), 1, 0, 1, ws, 1 << 20, plan, n1) == 2
+    assert lib.q4k_gemv_seq_plan(ok1, 1, 0, 1, None, 1 << 20, plan, n1) == 1          # no workspace
+    assert lib.q4k_gemv_seq_plan(ok1, 1, 0, 1, ws, 1 << 20, None, n1) == 1            # no plan
+    assert lib.q4k_gemv_seq_launch(None, None) == 1
+
+
 def test_status_strings_and_version(lib):
     assert lib.q4k_status_string(0) == b"Q4K_OK"
     assert lib.q4k_status_string(5) == b"Q4K_ERR_DEVICE_TIMEOUT"

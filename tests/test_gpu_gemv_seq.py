@@ -214,3 +214,41 @@ def test_36_layer_stack_in_one_launch(batch):
             y_ref, norm = O.gemv(slice_rows(fields[n], sample), xs[inp])
             assert_close(host(outs[L][n])[:, sample], y_ref, norm, f"stack layer {L} {n} b{batch}")
     assert q4k.q4k_device_error() == 0
+
+
+def test_plan_once_launch_many_with_new_inputs():
+    """q4k_gemv_seq_plan then q4k_gemv_seq_launch three times, the inputs
+    rewritten in place between launches (same buffers, new values), over a
+    list of 100 jobs (two launches per plan): each launch matches the oracle."""
+    cols, batch = 512, 1
+    shapes = [(64 + 8 * (i % 5), cols) for i in range(100)]
+    fields = [synth.q4k_fields(r, c, [900, i]) for i, (r, c) in enumerate(shapes)]
+    ws = [pack_dev(f) for f in fields]
+    xd = torch.empty((batch, cols), device="cuda")
+    ys = [torch.empty((batch, r), device="cuda") for r, _ in shapes]
+    jobs = [{"w": w, "rows": r, "cols": c, "x": xd, "y": y} for w, (r, c), y in zip(ws, shapes, ys)]
+    seq = q4k.GemvSeq(jobs, batch)
+    for rep in range(3):
+        x = synth.activations(batch, cols, [901, rep])
+        xd.copy_(torch.from_numpy(x))
+        seq()
+        torch.cuda.synchronize()
+        for i in (0, 37, 95, 96, 99):
+            y_ref, norm = O.gemv(fields[i], x)
+            ok, worst = O.within_tolerance(ys[i].cpu().numpy(), y_ref, norm, REL)
+            assert ok, f"rep {rep} job {i}: {worst:.3g}"
+    assert q4k.q4k_device_error() == 0
+
+
+def test_plan_and_one_shot_call_give_the_same_bits():
+    batch = 2
+    fields, xs = synth.decode_layer(synth.WL_DECODE_4B, 11, batch)
+    w = {n: pack_dev(fields[n]) for n in SHAPES}
+    xd = {k: dev(v) for k, v in xs.items()}
+    y1 = {n: torch.empty((batch, SHAPES[n][0]), device="cuda") for n in SHAPES}
+    y2 = {n: torch.empty((batch, SHAPES[n][0]), device="cuda") for n in SHAPES}
+    q4k.q4k_gemv_seq(layer_jobs(w, xd, y1, batch), batch)
+    q4k.GemvSeq(layer_jobs(w, xd, y2, batch), batch)()
+    torch.cuda.synchronize()
+    for n in SHAPES:
+        assert torch.equal(y1[n], y2[n]), n

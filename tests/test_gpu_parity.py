@@ -229,3 +229,33 @@ def test_gemm_prefill_512_sampled():
         toks = np.sort(rng.choice(512, 16, replace=False))
         y_ref, norm = O.mmq(f, rq[toks], rd[toks], rs[toks])
         assert_close(y[toks], y_ref, norm, f"{name} token sample")
+
+
+# ------------------------------------------------------------------ unpack
+@pytest.mark.parametrize("rows,cols", [(1, 256), (19, 768), (300, 2560)])
+def test_unpack_inverts_the_gpu_pack(rows, cols):
+    """Round trip on the GPU alone: the fields come back bit for bit
+    (q4k_unpack does not share the packer's code path)."""
+    f = synth.q4k_fields(rows, cols, [rows, cols, 5])
+    got = q4k.q4k_unpack(pack_dev(f), rows, cols)
+    torch.cuda.synchronize()
+    for k in ("d", "dmin"):
+        assert np.array_equal(got[k].cpu().numpy().view(np.uint16), f[k]), k
+    for k in ("sc", "m", "q"):
+        assert np.array_equal(got[k].cpu().numpy(), f[k]), k
+
+
+def test_unpack_reads_the_oracles_bytes():
+    """The GPU unpack of bytes packed by the oracle gives the oracle's fields,
+    and those match the oracle's own unpack."""
+    rows, cols = 40, 1024
+    f = synth.q4k_fields(rows, cols, 606)
+    packed = O.pack_block144(f)
+    w = torch.from_numpy(packed.reshape(-1)).cuda()
+    got = q4k.q4k_unpack(w, rows, cols)
+    ref = O.unpack_block144(packed)
+    torch.cuda.synchronize()
+    for k in ("d", "dmin"):
+        assert np.array_equal(got[k].cpu().numpy().view(np.uint16), ref[k]), k
+    for k in ("sc", "m", "q"):
+        assert np.array_equal(got[k].cpu().numpy(), ref[k]), k

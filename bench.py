@@ -550,9 +550,12 @@ def run_ours(args, rank, world):
     e2e_ms = e0.elapsed_time(e1)
 
     # ---------------- prefill GEMMs (q8_1 + MMQ)
-    def prefill_case(mats, xs_in, tokens, layers=1, rotate=True):
+    def prefill_case(mats, xs_in, tokens, layers=1, rotate=True, form="h16"):
         """mats: [(name, fields, rows, cols, input)].  Times one step = q8_1 of
-        every input + every GEMM, `layers` times over rotating weight copies."""
+        every input + every GEMM, `layers` times over rotating weight copies.
+        form "h16": q8_quantize_h16 + q4k_gemm_h16; "int8": q8_quantize + q4k_gemm."""
+        quant = q4k.q8_quantize_h16 if form == "h16" else q4k.q8_quantize
+        gemm = q4k.q4k_gemm_h16 if form == "h16" else q4k.q4k_gemm
         w = {}
         for name, f, rows, cols, inp in mats:
             d = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev) for k, v in f.items()}
@@ -561,7 +564,7 @@ def run_ours(args, rank, world):
         wbytes = sum(v.numel() for v in w.values())
         n_c = max(2, math.ceil(4 * l2 / wbytes)) if rotate else 1
         wsets = [w] + [{k: v.clone() for k, v in w.items()} for _ in range(n_c - 1)]
-        q8 = {k: q4k.q8_quantize(v) for k, v in x.items()}
+        q8 = {k: quant(v) for k, v in x.items()}
         y = {name: torch.empty((tokens, rows), device=dev) for name, _, rows, _, _ in mats}
 
         def step(gemm_only=False):
@@ -569,9 +572,9 @@ def run_ours(args, rank, world):
                 ws = wsets[L % n_c]
                 if not gemm_only:
                     for k, v in x.items():
-                        q4k.q8_quantize(v, *q8[k])
+                        quant(v, *q8[k])
                 for name, _, rows, cols, inp in mats:
-                    q4k.q4k_gemm(ws[name], rows, cols, *q8[inp], y=y[name])
+                    gemm(ws[name], rows, cols, *q8[inp], y=y[name])
 
         step()
         torch.cuda.synchronize()
@@ -581,7 +584,7 @@ def run_ours(args, rank, world):
         ms_gemm = time_graph(capture(lambda: step(True)), reps)
         launches = layers * (len(x) + len(mats))
         del wsets, w
-        return {"tokens": tokens, "ms_per_step": ms, "tok_s": tokens / (ms * 1e-3),
+        return {"tokens": tokens, "form": form, "ms_per_step": ms, "tok_s": tokens / (ms * 1e-3),
                 "int_tops": ops / (ms * 1e-3) / 1e12, "gemm_ms": ms_gemm,
                 "gemm_tops": ops / (ms_gemm * 1e-3) / 1e12, "gemm_frac_of_bf16": ops / (ms_gemm * 1e-3) / 1e12 / bf16,
                 "gpu_launches": launches, "l2": f"{n_c} rotating weight copies"}
@@ -590,12 +593,15 @@ def run_ours(args, rank, world):
     mats512 = [("gate", pf["gate"], 9728, 2560, "mlp_in"), ("down", pf["down"], 2560, 9728, "down_in")]
     prefill512 = prefill_case(mats512, pxs, 512)
     prefill512["workload"] = "512-token prefill: q8_1 X[512x2560] x gate 9728x2560, X_down[512x9728] x down 2560x9728"
+    p512_int8 = prefill_case(mats512, pxs, 512, form="int8")
+    prefill512["int8_entry_point"] = {k: p512_int8[k] for k in ("ms_per_step", "tok_s", "gemm_tops")}
     # short prompts (the pages' 18-33-token regime) on the same two matrices
     short = {}
     for T in (8, 16, 33, 64):
         sx = {k: np.ascontiguousarray(v[:T]) for k, v in pxs.items()}
-        r = prefill_case(mats512, sx, T)
-        short[f"tokens{T}"] = {k: r[k] for k in ("ms_per_step", "tok_s", "gemm_tops", "gemm_frac_of_bf16")}
+        for form in ("h16", "int8"):
+            r = prefill_case(mats512, sx, T, form=form)
+            short[f"tokens{T}_{form}"] = {k: r[k] for k in ("ms_per_step", "tok_s", "gemm_tops", "gemm_frac_of_bf16")}
     # 2048-token prefill of the 36-layer Qwen3-4B stack (7 projections a layer)
     x2048 = {name: synth.activations(2048, cols, synth.layer_seed(synth.WL_STACK_4B, 0, 300 + j))
              for j, (name, cols) in enumerate(synth.QWEN3_4B_INPUTS)}
@@ -706,8 +712,8 @@ def run_ours(args, rank, world):
                                  "peak is the dense fp16 = bf16 rate; sm_103a has no integer tcgen05 MMA",
                          "int8_peak_mma_sync_s8": int8_peak, "frac_of_int8_peak": prefill512["gemm_tops"] / int8_peak,
                          "tcgen05_f16_probe_tflops": f16_peak},
-            "timing": "median of CUDA-graph replays of exactly one step (q8_1 + GEMM for gate and down); "
-                      "gemm_tops from a graph of the GEMM launches alone",
+            "timing": "median of CUDA-graph replays of exactly one step (q8_quantize_h16 + q4k_gemm_h16 for "
+                      "gate and down); gemm_tops from a graph of the GEMM launches alone",
         },
         "prefill_short_prompts": short,
         "prefill_2048_stack": prefill2048,

@@ -143,6 +143,17 @@ int q8_quantize(const float* x, int64_t tokens, int64_t cols, int8_t* q,
                 float* d8, int32_t* sum, void* stream);
 
 /*
+ * q8_quantize_h16 - q8_quantize with the quants stored as binary16 values
+ * (every q is an integer in [-127, 127], exact in binary16): the operand
+ * form the tensor cores read, so q4k_gemm_h16 loads it without converting.
+ *   q : uint16 binary16 bits [tokens][cols]; d8, sum as for q8_quantize.
+ * Bit-exact: q holds exactly the values q8_quantize writes, d8 and sum are
+ * the same bits.
+ */
+int q8_quantize_h16(const float* x, int64_t tokens, int64_t cols, uint16_t* q,
+                    float* d8, int32_t* sum, void* stream);
+
+/*
  * q4k_gemv - decode GEMV (genie-ai-runtime §4, Path C: the hot decode
  * kernels; residual add folded into the GEMV):
  *   y[b][o] = sum_k w[o][k] * x[b][k]  (+ residual[b][o] if residual != NULL)
@@ -305,6 +316,17 @@ int q4k_gemm(const void* w, int layout, int64_t rows, int64_t cols,
              int64_t tokens, float* y, void* stream);
 
 /*
+ * q4k_gemm_h16 - q4k_gemm over q8_quantize_h16 output (the same MMQ form,
+ * results and accuracy); the fast prefill path: tensor copies load the
+ * binary16 quants straight into the tensor cores' operand layout.
+ *   q16 : uint16 binary16 quants [tokens][cols] (values -127..127)
+ * Other arguments as for q4k_gemm.
+ */
+int q4k_gemm_h16(const void* w, int layout, int64_t rows, int64_t cols,
+                 const uint16_t* q16, const float* d8, const int32_t* sum,
+                 int64_t tokens, float* y, void* stream);
+
+/*
  * q4k_gemm_blockdots - test export of the GEMM's per-block integer dots,
  * computed by the same tensor-core main loop as q4k_gemm:
  *   p[t][o][b] = sum_{i<32} q[o][32b+i] * q8[t][32b+i]
@@ -314,6 +336,12 @@ int q4k_gemm(const void* w, int layout, int64_t rows, int64_t cols,
 int q4k_gemm_blockdots(const void* w, int layout, int64_t rows, int64_t cols,
                        const int8_t* q8, int64_t tokens, int32_t* p,
                        void* stream);
+
+/* q4k_gemm_blockdots_h16 - the same test export from q4k_gemm_h16's main
+ * loop (binary16 quants q16 as for q4k_gemm_h16).  Bit-exact. */
+int q4k_gemm_blockdots_h16(const void* w, int layout, int64_t rows, int64_t cols,
+                           const uint16_t* q16, int64_t tokens, int32_t* p,
+                           void* stream);
 
 /*
  * q4k_device_error - synchronise `stream` and read (then clear) the

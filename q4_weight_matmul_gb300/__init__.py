@@ -42,6 +42,7 @@ SIGNATURES = {
     "q4k_unpack": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _P, _P, _P]),
     "q8_1_bytes": (ctypes.c_size_t, [_I64, _I64]),
     "q8_quantize": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "q8_quantize_h16": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q4k_gemv": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P, _P]),
     "q4k_gemv_multi": (_I, [_I, _P, _I, _P, _I64, _P, _I64, _P, _P, _P]),
     "q4k_gemv_seq_workspace_bytes": (ctypes.c_size_t, [_P, _I, _I64]),
@@ -52,6 +53,8 @@ SIGNATURES = {
     "q4k_gemv_seq_static": (_I, [_P, _I, _I, _I64, _P]),
     "q4k_gemm": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
     "q4k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
+    "q4k_gemm_h16": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
+    "q4k_gemm_blockdots_h16": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
     "q4k_device_error": (_I, [_P]),
     "q4k_selftest_wait_timeout": (_I, [_P]),
     "q4k_status_string": (ctypes.c_char_p, [_I]),
@@ -169,6 +172,20 @@ def q8_quantize(x, q=None, d8=None, s=None, stream=None):
     return q, d8, s
 
 
+def q8_quantize_h16(x, q=None, d8=None, s=None, stream=None):
+    """q8_1-quantise ``x`` with the quants as binary16 (torch.float16 holding
+    the integers -127..127); returns (q float16, d8 float32, sum int32)."""
+    tokens, cols = x.shape
+    dev = x.device
+    q = torch.empty((tokens, cols), dtype=torch.float16, device=dev) if q is None else q
+    d8 = torch.empty((tokens, cols // QK_SUB), dtype=torch.float32, device=dev) if d8 is None else d8
+    s = torch.empty((tokens, cols // QK_SUB), dtype=torch.int32, device=dev) if s is None else s
+    _check(lib().q8_quantize_h16(_ptr(x, torch.float32, "x"), tokens, cols, _ptr(q, torch.float16, "q"),
+                                 _ptr(d8, torch.float32, "d8"), _ptr(s, torch.int32, "sum"),
+                                 _stream(stream)), "q8_quantize_h16")
+    return q, d8, s
+
+
 def q4k_gemv(w, rows: int, cols: int, x, residual=None, y=None, layout: int = BLOCK144, stream=None):
     """Decode GEMV: ``y[b] = W x[b] (+ residual[b])`` for ``x`` [batch][cols] float32."""
     batch = x.shape[0]
@@ -282,6 +299,30 @@ def q4k_gemm(w, rows: int, cols: int, q8, d8, s, y=None, layout: int = BLOCK144,
     return y
 
 
+def q4k_gemm_h16(w, rows: int, cols: int, q16, d8, s, y=None, layout: int = BLOCK144, stream=None):
+    """Prefill MMQ GEMM on ``q8_quantize_h16`` output; returns ``y`` [tokens][rows] float32."""
+    tokens = q16.shape[0]
+    if y is None:
+        y = torch.empty((tokens, rows), dtype=torch.float32, device=q16.device)
+    _check(lib().q4k_gemm_h16(_ptr(w, torch.uint8, "w"), layout, rows, cols,
+                              _ptr(q16, torch.float16, "q16"), _ptr(d8, torch.float32, "d8"),
+                              _ptr(s, torch.int32, "sum"), tokens, _ptr(y, torch.float32, "y"),
+                              _stream(stream)), "q4k_gemm_h16")
+    return y
+
+
+def q4k_gemm_blockdots_h16(w, rows: int, cols: int, q16, p=None, layout: int = BLOCK144, stream=None):
+    """Test export: q4k_gemm_h16's exact per-block integer dots, int32 [tokens][rows][cols/32]."""
+    tokens = q16.shape[0]
+    if p is None:
+        p = torch.empty((tokens, rows, cols // QK_SUB), dtype=torch.int32, device=q16.device)
+    _check(lib().q4k_gemm_blockdots_h16(_ptr(w, torch.uint8, "w"), layout, rows, cols,
+                                        _ptr(q16, torch.float16, "q16"), tokens,
+                                        _ptr(p, torch.int32, "p"), _stream(stream)),
+           "q4k_gemm_blockdots_h16")
+    return p
+
+
 def q4k_gemm_blockdots(w, rows: int, cols: int, q8, p=None, layout: int = BLOCK144, stream=None):
     """Test export: the GEMM's exact per-block integer dots, int32 [tokens][rows][cols/32]."""
     tokens = q8.shape[0]
@@ -310,7 +351,7 @@ def q4k_version() -> str:
 
 
 __all__ = ["build", "lib", "Q4KError", "BLOCK144", "LAYOUT_GPU", "q4k_packed_bytes", "q4k_pack", "q4k_unpack",
-           "q8_1_bytes", "q8_quantize",
+           "q8_1_bytes", "q8_quantize", "q8_quantize_h16", "q4k_gemm_h16", "q4k_gemm_blockdots_h16",
            "q4k_gemv", "q4k_gemv_multi", "GemvJob", "GemvSeq", "q4k_gemv_seq", "q4k_gemv_seq_static", "q4k_gemm",
            "q4k_gemm_blockdots", "q4k_device_error",
            "q4k_selftest_wait_timeout", "q4k_version",

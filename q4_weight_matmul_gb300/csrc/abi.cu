@@ -74,21 +74,42 @@ int* device_error_word() {
   return g_error_ptr[dev];
 }
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return nullptr;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return encode;
+}
+}  // namespace
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0,
+                    uint64_t dim1, uint64_t row_stride_bytes, uint32_t box0, uint32_t box1,
+                    CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (!encode) return false;
+  const cuuint64_t gdim[2] = {dim0, dim1};
+  const cuuint64_t gstride[1] = {row_stride_bytes};
+  const cuuint32_t bdim[2] = {box0, box1};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult r = encode(map, dtype, 2, const_cast<void*>(base), gdim, gstride, bdim, estride,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool encode_tmap_u8_3d(CUtensorMap* map, const void* base, const uint64_t dims[3],
                        const uint64_t strides[2], const uint32_t box[3]) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-              cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || !fn)
-        return false;
-      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  }
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (!encode) return false;
   const cuuint64_t gdim[3] = {dims[0], dims[1], dims[2]};
   const cuuint64_t gstride[2] = {strides[0], strides[1]};
   const cuuint32_t bdim[3] = {box[0], box[1], box[2]};
@@ -153,6 +174,17 @@ int q8_quantize(const float* x, int64_t tokens, int64_t cols, int8_t* q, float* 
   if (!x || !q || !d8 || !sum) return Q4K_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(q) || !aligned16(d8) || !aligned16(sum)) return Q4K_ERR_ALIGNMENT;
   cudaError_t e = launch_q8_quantize(x, tokens, cols, q, d8, sum, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+int q8_quantize_h16(const float* x, int64_t tokens, int64_t cols, uint16_t* q, float* d8, int32_t* sum,
+                    void* stream) {
+  if (tokens < 0 || tokens > (int64_t(1) << 24)) return Q4K_ERR_INVALID_ARG;
+  if (int e = check_cols(cols)) return e;
+  if (tokens == 0) return Q4K_OK;
+  if (!x || !q || !d8 || !sum) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(d8) || !aligned16(sum)) return Q4K_ERR_ALIGNMENT;
+  cudaError_t e = launch_q8_quantize_h16(x, tokens, cols, q, d8, sum, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? Q4K_OK : record_cuda(e);
 }
 
@@ -263,6 +295,37 @@ int q4k_gemm_blockdots(const void* w, int layout, int64_t rows, int64_t cols, co
                        int64_t tokens, int32_t* p, void* stream) {
   if (!p && rows != 0 && tokens != 0) return Q4K_ERR_INVALID_ARG;
   return gemm_common(w, layout, rows, cols, q8, nullptr, nullptr, tokens, nullptr, p, stream);
+}
+
+static int gemm_h16_common(const void* w, int layout, int64_t rows, int64_t cols, const uint16_t* q16,
+                           const float* d8, const int32_t* sum, int64_t tokens, float* y, int32_t* p,
+                           void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_layout(layout)) return e;
+  if (tokens < 0 || tokens > (int64_t(1) << 22)) return Q4K_ERR_INVALID_ARG;
+  if (rows == 0 || tokens == 0) return Q4K_OK;
+  if (!w || !q16) return Q4K_ERR_INVALID_ARG;
+  if (!p && (!d8 || !sum || !y)) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(q16) || (d8 && !aligned16(d8)) || (sum && !aligned16(sum)) ||
+      (y && !aligned16(y)) || (p && !aligned16(p)))
+    return Q4K_ERR_ALIGNMENT;
+  int* err = device_error_word();
+  if (!err) return record_cuda(cudaGetLastError());
+  cudaError_t e = launch_gemm_h16(static_cast<const uint8_t*>(w), rows, cols, q16, d8, sum, tokens, y, p, err,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+int q4k_gemm_h16(const void* w, int layout, int64_t rows, int64_t cols, const uint16_t* q16, const float* d8,
+                 const int32_t* sum, int64_t tokens, float* y, void* stream) {
+  return gemm_h16_common(w, layout, rows, cols, q16, d8, sum, tokens, y, nullptr, stream);
+}
+
+int q4k_gemm_blockdots_h16(const void* w, int layout, int64_t rows, int64_t cols, const uint16_t* q16,
+                           int64_t tokens, int32_t* p, void* stream) {
+  if (!p && rows != 0 && tokens != 0) return Q4K_ERR_INVALID_ARG;
+  return gemm_h16_common(w, layout, rows, cols, q16, nullptr, nullptr, tokens, nullptr, p, stream);
 }
 
 size_t q4k_gemv_seq_workspace_bytes(const q4k_gemv_job* jobs, int n_jobs, int64_t batch) {

@@ -131,8 +131,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
       tc::mbar_init(&empty[i], SB);
     }
     *issued = 0;
-    int* pc = gemv::pool_counter(xss);
-    pc[0] = pc[1] = pc[2] = pc[3] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -176,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
 
   // -------------------------------------------------------------- consumers
   if (P.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
-  gemv::stage_x<B, kConsumers, false>(P.x, nb, xs, xss, tid, 0);
+  gemv::stage_x<B, kConsumers, false>(P.x, nb, xs, xss, tid);
   named_sync_consumers();
   const gemv::XView xv = gemv::make_view(xs, xss, P.x, B, nb);
 

@@ -10,9 +10,9 @@
 // signed byte in [-128, 127].  The 4-bit quants q enter dp4a dot products with
 // the digit planes unchanged, so each plane sum sum(q*D) is an exact integer
 // of magnitude <= 15*128*32, and so is every pair 256*P_hi + P_lo of them; a
-// sub-block's value is then formed as
+// sub-block's value is then formed with a single fp32 rounding:
 //     tier 1:  P/256 ~ fmaf(256*P3 + P2, 256, P1)            (D0 dropped)
-//     tier 2:  the same, plus P0/256 added as a second term
+//     tier 2:  P/256 = fmaf(256*P3 + P2, 256, (256*P1 + P0)/256)
 // and the scales are applied in fp32 registers:
 //     acc += d*sc_j*s'_j*V_j - dmin*m_j*XS_j,   s'_j = 256*s_j, XS_j = sum x.
 // Balanced digits keep every plane sum within twice sum q|X|, so combining
@@ -23,14 +23,16 @@
 //  - tier 1 (three planes D3..D1): every element keeps |x - s'*X'| <= 2^-14 |x|;
 //  - tier 2 (all four planes): some element would not, but every nonzero
 //    element keeps |x - s*X| <= 2^-14 |x| (a wide range inside the block);
+//    D0 is added as a second exact integer term of the same rounding;
 //  - tier 3 (fp32): any other block -- an element below ~2^-16 of the
 //    block's largest, or a largest |x| outside [2^-87, 2^94) -- is staged
 //    with scale 0 (and its fp32 activations in a small pool) and takes
 //    V_j = sum q*x by fp32 multiply-adds after the integer loop.
-// A 32-bit word of quants (8 weights) costs a shift, two LOP3s and six dp4a
-// per token (tier 2 adds a pass of one dp4a per 4 weights over its
-// sub-blocks), against one fp32 multiply-add per weight for a dequantised
-// dot.
+// Tier-2 sub-blocks keep their D0 plane in a small per-warp pool of shared
+// memory; a chunk holding one takes one extra warp-uniform branch.  A 32-bit
+// word of quants (8 weights) costs a shift, two LOP3s and six dp4a per token
+// (plus two dp4a in a tier-2 sub-block), against one fp32 multiply-add per
+// weight for a dequantised dot.
 #pragma once
 
 #include "q4k_internal.h"
@@ -42,9 +44,9 @@
 namespace q4k {
 namespace gemv {
 
-constexpr int kRegion = 208;   // bytes per (token, superblock, chunk) of the planes D3..D1: 192 + pad
-constexpr int kPoolMax = 256;  // D0 planes of tier-2 sub-blocks a CTA holds (32 bytes each)
-constexpr int kPool3Max = 32;  // fp32 activations of tier-3 sub-blocks a CTA holds (128 bytes each)
+constexpr int kRegion = 208;     // bytes per (token, superblock, chunk) of the planes D3..D1: 192 + pad
+constexpr int kStageWarps = 15;  // warps that stage x (the consumer warps of both kernels)
+constexpr int kPool3PerWarp = 1; // fp32 activations of tier-3 sub-blocks a warp keeps (128 bytes each)
 constexpr uint32_t kNoSlot = 0x3FFFu;   // a tier-3 sub-block without a pool slot reads x from global memory
 // biased fp32 exponents of a sub-block's largest |x| staged in fixed point
 constexpr int kEFixedMin = 40;    // 2^-87
@@ -79,22 +81,23 @@ __device__ __noinline__ inline bool wait_issued(volatile int* issued, int j) {
 }
 
 // Shared-memory bytes of the staged activations: the planes D3..D1 (xs),
-// then (xss) the pool counters, the (scale, sum) pair and the tag of every
-// sub-block, the pool of D0 planes and the pool of tier-3 activations.  Only the counters sit at a fixed
-// offset; the rest is laid out for the nb being staged.
-__host__ __device__ constexpr int pool_entries(int B, int nb) { return B * nb * 8 < kPoolMax ? B * nb * 8 : kPoolMax; }
-__host__ __device__ constexpr int pool3_entries(int B, int nb) { return B * nb * 8 < kPool3Max ? B * nb * 8 : kPool3Max; }
-__host__ __device__ constexpr size_t ss_offset() { return 16; }
-__host__ __device__ constexpr size_t tag_offset(int B, int nb) { return 16 + sizeof(float2) * (size_t)B * nb * 8; }
-__host__ __device__ constexpr size_t pool_offset(int B, int nb) {
+// then (xss) the (scale, sum) pair and the tag of every sub-block, the D0
+// pool (per warp: pool2_per_warp slots of 32 bytes) and the tier-3 pool (per
+// warp: kPool3PerWarp slots of 128 bytes).  Laid out for the nb being staged.
+__host__ __device__ constexpr int pool2_per_warp(int B, int nb) {
+  // about a quarter of a warp's sub-blocks; N(0,1) activations need ~9 %
+  return (B * nb * 8 + 59) / 60 < 2 ? 2 : ((B * nb * 8 + 59) / 60 > 16 ? 16 : (B * nb * 8 + 59) / 60);
+}
+__host__ __device__ constexpr size_t tag_offset(int B, int nb) { return sizeof(float2) * (size_t)B * nb * 8; }
+__host__ __device__ constexpr size_t pool2_offset(int B, int nb) {
   return (tag_offset(B, nb) + sizeof(uint16_t) * (size_t)B * nb * 8 + 15) & ~size_t(15);
 }
-__host__ __device__ constexpr size_t xs_bytes(int B, int nb) { return (size_t)B * nb * 4 * kRegion; }
 __host__ __device__ constexpr size_t pool3_offset(int B, int nb) {
-  return pool_offset(B, nb) + 32 * (size_t)pool_entries(B, nb);
+  return pool2_offset(B, nb) + 32 * (size_t)kStageWarps * pool2_per_warp(B, nb);
 }
+__host__ __device__ constexpr size_t xs_bytes(int B, int nb) { return (size_t)B * nb * 4 * kRegion; }
 __host__ __device__ constexpr size_t xss_bytes(int B, int nb) {
-  return pool3_offset(B, nb) + 128 * (size_t)pool3_entries(B, nb);
+  return pool3_offset(B, nb) + 128 * (size_t)kStageWarps * kPool3PerWarp;
 }
 
 // Staged activations as the consumers read them.
@@ -102,36 +105,24 @@ struct XView {
   const uint8_t* planes;   // [B][nb][4 chunks][kRegion]: planes D3..D1
   const float2* ss;        // [B][nb][8]: (scale s', fp32 sum of x); s' = 0 in tier 3
   const uint16_t* tag;     // [B][nb][8]: bits 0-1 tier-1 (0), -2 (1) or -3 (2); bits 2.. pool slot
-  const uint8_t* pool;     // [slot][32]: the D0 plane of a tier-2 sub-block
+  const uint8_t* pool2;    // [slot][32]: the D0 plane of a tier-2 sub-block
   const float* pool3;      // [slot][32]: the activations of a tier-3 sub-block
-  const float* x;          // the activations themselves, [B][nb*256] (tier 3)
+  const float* x;          // the activations themselves, [B][nb*256] (tier 3 without a slot)
   int nb;
-};
-
-struct XSmem {
-  uint16_t* tag;
-  uint8_t* pool;
-  int* count;
 };
 
 __device__ __forceinline__ XView make_view(const uint8_t* xs, const float2* xss, const float* x, int B, int nb) {
   const uint8_t* base = reinterpret_cast<const uint8_t*>(xss);
   XView v;
   v.planes = xs;
-  v.ss = reinterpret_cast<const float2*>(base + ss_offset());
+  v.ss = xss;
   v.tag = reinterpret_cast<const uint16_t*>(base + tag_offset(B, nb));
-  v.pool = base + pool_offset(B, nb);
+  v.pool2 = base + pool2_offset(B, nb);
   v.pool3 = reinterpret_cast<const float*>(base + pool3_offset(B, nb));
   v.x = x;
   v.nb = nb;
   return v;
 }
-
-// The pool counters that stage_x allocates slots from: counter[gen & 1] for
-// the D0 pool and counter[2 + (gen & 1)] for the tier-3 pool in staging
-// number `gen`; stage_x zeroes the other two for the next staging.  Zero all
-// four before the first stage_x.
-__device__ __forceinline__ int* pool_counter(float2* xss) { return reinterpret_cast<int*>(xss); }
 
 // byte k (0..3) of each of four words, gathered into one word
 __device__ __forceinline__ uint32_t gather_byte(uint32_t a, uint32_t b, uint32_t c, uint32_t d, int k) {
@@ -143,35 +134,30 @@ __device__ __forceinline__ uint32_t gather_byte(uint32_t a, uint32_t b, uint32_t
 // point, with each sub-block's scale, fp32 sum and tier.  Eight lanes hold
 // one sub-block (four elements each), so its max and sum are three shuffles
 // and its tier one ballot; all loads of a round are issued before any use.
-// NT threads (a multiple of 32, tid < NT) take part; `gen` numbers the
-// stagings of one CTA (0, 1, 2, ...), and the pool counter of this one
-// (pool_counter) must be zero when they enter.  kCoherent reads x through L2 only (x may have
-// been written earlier in the same kernel); otherwise through the read-only
-// path.
+// NT = 32 * kStageWarps threads (tid < NT) take part.  Each warp hands out
+// the pool slots of the sub-blocks it stages from its own share of the
+// pools, counting in registers (two ballots per round, no atomics); a tier-2 sub-block that finds the warp's share full goes to
+// tier 3, and a tier-3 one without a slot reads x from global memory.
+// kCoherent reads x through L2 only (x may have been written earlier in the
+// same kernel); otherwise through the read-only path.
 // Plane layout per (token, superblock, chunk c): 16-byte words at
 // ((h*3 + p)*2 + s)*16, h = half of the chunk's 32 positions, p = plane
 // (0, 1, 2 = digits D1, D2, D3), s = sub-block 2c (0) or 2c+1 (1); word k of
-// it holds positions 16h+4k..+3.  A tier-2 sub-block's D0 plane takes a
-// pool slot of 32 bytes (word k: positions 4k..4k+3); when the pool is full
-// the sub-block goes to tier 3 instead.
+// it holds positions 16h+4k..+3.  A D0 pool slot (32 bytes) holds positions
+// 4k..4k+3 in word k.
 template <int B, int NT, bool kCoherent>
 __device__ __forceinline__ void stage_x(const float* __restrict__ x, int nb, uint8_t* xs, float2* xss,
-                                        int tid, int gen) {
+                                        int tid) {
+  static_assert(NT == 32 * kStageWarps, "pools are laid out per staging warp");
   uint8_t* xb = reinterpret_cast<uint8_t*>(xss);
-  float2* ssv = reinterpret_cast<float2*>(xb + ss_offset());
   uint16_t* tag = reinterpret_cast<uint16_t*>(xb + tag_offset(B, nb));
-  uint32_t* pool = reinterpret_cast<uint32_t*>(xb + pool_offset(B, nb));
-  float* pool3 = reinterpret_cast<float*>(xb + pool3_offset(B, nb));
-  int* pool_count = pool_counter(xss) + (gen & 1);
-  int* pool3_count = pool_counter(xss) + 2 + (gen & 1);
-  if (tid == 0) {
-    pool_counter(xss)[(gen + 1) & 1] = 0;
-    pool_counter(xss)[2 + ((gen + 1) & 1)] = 0;
-  }
-  const int pool_cap = pool_entries(B, nb), pool3_cap = pool3_entries(B, nb);
-  const int lane = tid & 31;
-  const int row4 = nb * 64;                     // float4 per activation row
-  const int n4 = B * row4;                      // a multiple of 64: whole warps
+  uint32_t* pool2 = reinterpret_cast<uint32_t*>(xb + pool2_offset(B, nb));
+  float4* pool3 = reinterpret_cast<float4*>(xb + pool3_offset(B, nb));
+  const int lane = tid & 31, warp = tid >> 5;
+  const int cap2 = pool2_per_warp(B, nb);
+  int used2 = 0, used3 = 0;                          // warp-uniform
+  const int row4 = nb * 64;                          // float4 per activation row
+  const int n4 = B * row4;                           // a multiple of 64: whole warps
   const float4* x4 = reinterpret_cast<const float4*>(x);
   for (int base = tid; base < n4; base += 5 * NT) {
     float4 v[5];
@@ -218,28 +204,47 @@ __device__ __forceinline__ void stage_x(const float* __restrict__ x, int nb, uin
                         (h * 3 * 2 + sf) * 4 + kw;
 #pragma unroll
         for (int pl = 0; pl < 3; ++pl) dst[pl * 2 * 4] = gather_byte(dg[0], dg[1], dg[2], dg[3], pl + 1);
-        // a sub-block's tier: any of its eight lanes; tier 2 takes a pool slot
+        // a sub-block's tier: any of its eight lanes.  From the two ballots
+        // every lane derives the warp's four groups' tiers, so the pool slots
+        // (in group order) need no further exchange.
         const unsigned b2 = __ballot_sync(0xffffffffu, t2), b3 = __ballot_sync(0xffffffffu, t3);
         const int grp = lane & 24;
-        const bool g2 = ((b2 >> grp) & 0xFFu) != 0;
-        bool g3 = ((b3 >> grp) & 0xFFu) != 0;
-        int slot = 0;
-        if ((idx & 7) == 0 && g2 && !g3) slot = atomicAdd(pool_count, 1);
-        slot = __shfl_sync(0xffffffffu, slot, grp);
-        if (g2 && !g3) {
-          if (slot < pool_cap) pool[(size_t)slot * 8 + (pos >> 2)] = gather_byte(dg[0], dg[1], dg[2], dg[3], 0);
-          else g3 = true;
+        unsigned want2 = 0u, want3 = 0u;   // bit g: group g takes a slot of the pool
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const bool g3g = ((b3 >> (8 * g)) & 0xFFu) != 0, g2g = !g3g && ((b2 >> (8 * g)) & 0xFFu) != 0;
+          want2 |= (g2g ? 1u : 0u) << g;
+          want3 |= (g3g ? 1u : 0u) << g;
         }
-        // a tier-3 sub-block keeps its fp32 activations in the pool if it can
-        int slot3 = 0;
-        if ((idx & 7) == 0 && g3) slot3 = atomicAdd(pool3_count, 1);
-        slot3 = __shfl_sync(0xffffffffu, slot3, grp);
-        if (g3 && slot3 < pool3_cap) reinterpret_cast<float4*>(pool3 + (size_t)slot3 * 32)[pos >> 2] = v[u];
+        const int gi = grp >> 3;
+        const unsigned before = (1u << gi) - 1u;
+        const bool g2 = (want2 >> gi) & 1u;
+        const int slot2 = used2 + __popc(want2 & before);
+        const bool in2 = g2 && slot2 < cap2;
+        // tier-2 groups beyond the warp's share of the pool go to tier 3
+        unsigned over = 0u;
+        {
+          int k = used2;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            if ((want2 >> g) & 1u) {
+              if (k >= cap2) over |= 1u << g;
+              ++k;
+            }
+        }
+        used2 += __popc(want2);
+        want3 |= over;
+        const bool g3 = (want3 >> gi) & 1u;
+        const int slot3 = used3 + __popc(want3 & before);
+        used3 += __popc(want3);
+        const bool in3 = g3 && slot3 < kPool3PerWarp;
+        const int s2 = warp * cap2 + slot2, s3 = warp * kPool3PerWarp + slot3;
+        if (in2) pool2[(size_t)s2 * 8 + (pos >> 2)] = gather_byte(dg[0], dg[1], dg[2], dg[3], 0);
+        if (in3) pool3[(size_t)s3 * 8 + (pos >> 2)] = v[u];
         if ((idx & 7) == 0) {
           const size_t e = ((size_t)b * nb + sb) * 8 + j;
-          ssv[e] = make_float2(g3 ? 0.0f : s24, sum);
-          const uint32_t s3 = slot3 < pool3_cap ? (uint32_t)slot3 : kNoSlot;
-          tag[e] = (uint16_t)(g3 ? 2u | (s3 << 2) : (g2 ? 1u | ((uint32_t)slot << 2) : 0u));
+          xss[e] = make_float2(g3 ? 0.0f : s24, sum);
+          tag[e] = (uint16_t)(g3 ? 2u | ((in3 ? (uint32_t)s3 : kNoSlot) << 2) : (in2 ? 1u | ((uint32_t)s2 << 2) : 0u));
         }
       }
     }
@@ -267,48 +272,23 @@ __device__ __forceinline__ float subblock_fp32(const uint8_t* p, int j, const fl
   return v;
 }
 
-// Tier-2 correction of sub-block j of the BLOCK144 superblock at `p`: the
-// exact integer sum of q * D0 (the fourth digit plane, a 32-byte pool entry)
-// over its 32 weights.
-__device__ __forceinline__ int subblock_plane0(const uint8_t* p, int j, const uint8_t* d0) {
-  const uint8_t* qs = p + 16 + 32 * (j >> 1);
-  const int hi = j & 1;
-  int acc = 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint4 qq = *reinterpret_cast<const uint4*>(qs + 16 * h);
-    const uint4 xw = reinterpret_cast<const uint4*>(d0)[h];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t w = word_of(qq, k);
-      acc = dp4a_us(hi ? (w >> 4) & 0x0F0F0F0Fu : w & 0x0F0F0F0Fu, word_of(xw, k), acc);
-    }
-  }
-  return acc;
-}
-
-// What tier-2 and tier-3 sub-blocks among chunks c0 .. c0+cpl-1 add to the
-// lane's scaled sum for token b: sc_j s'_j (sum q*D0) / 256 for tier 2;
-// sc_j sum q*x in fp32, straight from x, for tier 3 (staged with scale 0, so
-// the planes added nothing).  Out of line: the main loop keeps its registers.
+// What the tier-3 sub-blocks among chunks c0 .. c0+cpl-1 add to the lane's
+// scaled sum for token b: sc_j * sum q*x in fp32 (they were staged with scale
+// 0, so the planes added nothing).  Out of line: rare, and the main loop
+// keeps its registers.
 template <bool kCoherent>
-__device__ __noinline__ float tier_fix(const uint8_t* p, const XView X, int sb, int c0, int cpl, int b,
-                                       uint32_t sc03, uint32_t sc47) {
+__device__ __noinline__ float tier3_fix(const uint8_t* p, const XView X, int sb, int c0, int cpl, int b,
+                                        uint32_t sc03, uint32_t sc47) {
   const int nb = X.nb;
   const uint16_t* tg = X.tag + ((size_t)b * nb + sb) * 8;
-  const float2* ssb = X.ss + ((size_t)b * nb + sb) * 8;
   float add = 0.0f;
   for (int j = 2 * c0; j < 2 * (c0 + cpl); ++j) {
     const uint32_t t = tg[j];
-    if (!(t & 3u)) continue;
+    if (!(t & 2u)) continue;
     const float sc = byte_f(j < 4 ? sc03 : sc47, j & 3);
-    if (t & 2u) {
-      const float* xg = X.x + (size_t)b * nb * 256 + (size_t)sb * 256 + 32 * j;
-      const float* xs = (t >> 2) != kNoSlot ? X.pool3 + 32 * (size_t)(t >> 2) : nullptr;
-      add = fmaf(sc, subblock_fp32<kCoherent>(p, j, xs, xg), add);
-    } else {
-      add = fmaf(sc * ssb[j].x, (float)subblock_plane0(p, j, X.pool + 32 * (size_t)(t >> 2)) * 0.00390625f, add);
-    }
+    const float* xg = X.x + (size_t)b * nb * 256 + (size_t)sb * 256 + 32 * j;
+    const float* xs = (t >> 2) != kNoSlot ? X.pool3 + 32 * (size_t)(t >> 2) : nullptr;
+    add = fmaf(sc, subblock_fp32<kCoherent>(p, j, xs, xg), add);
   }
   return add;
 }
@@ -317,10 +297,8 @@ __device__ __noinline__ float tier_fix(const uint8_t* p, const XView X, int sb, 
 // chunks c0 .. c0+CPL-1 (64 weights each) of the BLOCK144 superblock at `p`
 // (shared memory), superblock index sb of x.  acc[b] receives
 // d * sum_j sc_j s'_j V_j - dmin * sum_j m_j XS_j over the lane's sub-blocks.
-// The main loop takes the three planes D3..D1 of every sub-block, with no
-// branch; tier-2 and tier-3 sub-blocks are completed after it (tier_fix).
-// With balanced digits every partial value is within twice sum q|X|, so
-// adding the D0 term as a separately rounded term costs at most 2^-22 of that.
+// Per chunk the three planes D3..D1 of both sub-blocks, then, only where a
+// sub-block is in tier 2, its D0 plane; tier-3 sub-blocks are added after.
 template <int B, int CPL, bool kCoherent>
 __device__ __forceinline__ void superblock_dot(const uint8_t* p, const XView& X, int sb, int c0,
                                                float (&acc)[B]) {
@@ -378,9 +356,30 @@ __device__ __forceinline__ void superblock_dot(const uint8_t* p, const XView& X,
     const float m_lo = byte_f(mw, bi), m_hi = byte_f(mw, bi + 1);
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-      // (P - D0 term) / 256 in units of s' = 256 s, one rounding
-      const float v_lo = fmaf((float)(lo[b][2] * 256 + lo[b][1]), 256.0f, (float)lo[b][0]);
-      const float v_hi = fmaf((float)(hi[b][2] * 256 + hi[b][1]), 256.0f, (float)hi[b][0]);
+      // tier 2: the D0 planes of the chunk's flagged sub-blocks, from the pool
+      const uint32_t tw = *reinterpret_cast<const uint32_t*>(X.tag + ((size_t)b * nb + sb) * 8 + 2 * c);
+      int p0_lo = 0, p0_hi = 0;
+      if (tw & 0x00010001u) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 qq = h ? q1 : q0;
+          if ((tw & 3u) == 1u) {
+            const uint4 xw = reinterpret_cast<const uint4*>(X.pool2 + 32 * (size_t)((tw >> 2) & 0x3FFFu))[h];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) p0_lo = dp4a_us(word_of(qq, k) & 0x0F0F0F0Fu, word_of(xw, k), p0_lo);
+          }
+          if (((tw >> 16) & 3u) == 1u) {
+            const uint4 xw = reinterpret_cast<const uint4*>(X.pool2 + 32 * (size_t)(tw >> 18))[h];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              p0_hi = dp4a_us((word_of(qq, k) >> 4) & 0x0F0F0F0Fu, word_of(xw, k), p0_hi);
+          }
+        }
+      }
+      // P/256 in units of s' = 256 s, one rounding (exact integer parts;
+      // without tier 2, p0 = 0 and the second term is the integer P1)
+      const float v_lo = fmaf((float)(lo[b][2] * 256 + lo[b][1]), 256.0f, (float)(lo[b][0] * 256 + p0_lo) * 0.00390625f);
+      const float v_hi = fmaf((float)(hi[b][2] * 256 + hi[b][1]), 256.0f, (float)(hi[b][0] * 256 + p0_hi) * 0.00390625f);
       const float4 ss = *reinterpret_cast<const float4*>(X.ss + ((size_t)b * nb + sb) * 8 + 2 * c);
       scaled[b] = fmaf(sc_hi * ss.z, v_hi, fmaf(sc_lo * ss.x, v_lo, scaled[b]));
       mins[b] = fmaf(m_hi, ss.w, fmaf(m_lo, ss.y, mins[b]));
@@ -388,7 +387,7 @@ __device__ __forceinline__ void superblock_dot(const uint8_t* p, const XView& X,
   }
 #pragma unroll
   for (int b = 0; b < B; ++b) acc[b] = fmaf(dm.x, scaled[b], -dm.y * mins[b]);
-  // tier-2 and tier-3 sub-blocks among the lane's chunks
+  // tier-3 sub-blocks among the lane's chunks (rare)
 #pragma unroll
   for (int b = 0; b < B; ++b) {
     // the tags of the lane's sub-blocks 2c0 .. 2(c0+CPL)-1, two per word
@@ -397,7 +396,7 @@ __device__ __forceinline__ void superblock_dot(const uint8_t* p, const XView& X,
     if (CPL == 4) any = t8.x | t8.y | t8.z | t8.w;
     else if (CPL == 2) any = c0 ? (t8.z | t8.w) : (t8.x | t8.y);
     else any = word_of(t8, c0);
-    if (any & 0x00030003u) acc[b] = fmaf(dm.x, tier_fix<kCoherent>(p, X, sb, c0, CPL, b, sc03, sc47), acc[b]);
+    if (any & 0x00020002u) acc[b] = fmaf(dm.x, tier3_fix<kCoherent>(p, X, sb, c0, CPL, b, sc03, sc47), acc[b]);
   }
 }
 

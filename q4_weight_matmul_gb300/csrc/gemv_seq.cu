@@ -318,8 +318,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
     }
     *issued = 0;
     flags[0] = flags[1] = flags[2] = 0;
-    int* pc = gemv::pool_counter(xss);
-    pc[0] = pc[1] = pc[2] = pc[3] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -381,7 +379,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
   const float* staged_x = nullptr;
   int staged_nb = -1;
   int J = 0;          // this CTA's stages so far (ring order)
-  int n_staged = 0;   // activation stagings so far (pool counter generation)
   int pass_no = 0;
   constexpr int per = kRB * B;
   for (int ei = 0; ei < P.n_epoch; ++ei) {
@@ -410,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
       const long long u0 = u - S.unit_base, u1 = (e1 < su1 ? e1 : su1) - S.unit_base;   // segment units
       const int n_units = (int)(u1 - u0);
       if (S.x != staged_x || nb != staged_nb) {
-        gemv::stage_x<B, kConsumers, true>(S.x, nb, xs, xss, tid, n_staged++);
+        gemv::stage_x<B, kConsumers, true>(S.x, nb, xs, xss, tid);
         staged_x = S.x;
         staged_nb = nb;
         named_sync_consumers();

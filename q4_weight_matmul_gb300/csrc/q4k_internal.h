@@ -36,6 +36,9 @@ cudaError_t launch_unpack_block144(const uint8_t* w, int64_t rows, int64_t cols,
 cudaError_t launch_q8_quantize(const float* x, int64_t tokens, int64_t cols,
                                int8_t* q, float* d8, int32_t* sum,
                                cudaStream_t s);
+// The same quantisation with the quants stored as exact binary16 integers.
+cudaError_t launch_q8_quantize_h16(const float* x, int64_t tokens, int64_t cols, uint16_t* q, float* d8,
+                                   int32_t* sum, cudaStream_t s);
 
 // Decode GEMV over n_mats (1..gemv_max_mats()) matrices that share one input
 // x; matrix m has rows[m] rows, output y[m] and optional residual[m].
@@ -78,6 +81,12 @@ cudaError_t launch_gemm_block144(const uint8_t* w, int64_t rows, int64_t cols,
                                  const int8_t* q8, const float* d8,
                                  const int32_t* sum, int64_t tokens, float* y,
                                  int32_t* p_out, int* err, cudaStream_t s);
+
+// Tensor-core prefill MMQ GEMM over binary16 quants (tensor copies load the
+// activation operand directly).  p_out as for launch_gemm_block144.
+cudaError_t launch_gemm_h16(const uint8_t* w, int64_t rows, int64_t cols, const uint16_t* q16, const float* d8,
+                            const int32_t* sum, int64_t tokens, float* y, int32_t* p_out, int* err,
+                            cudaStream_t s);
 
 // One-thread kernel whose only (bounded) wait can never complete: after the
 // library's wait limit it records a timeout in `err` and returns.

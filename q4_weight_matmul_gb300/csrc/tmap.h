@@ -13,4 +13,10 @@ namespace q4k {
 bool encode_tmap_u8_3d(CUtensorMap* map, const void* base, const uint64_t dims[3],
                        const uint64_t strides[2], const uint32_t box[3]);
 
+// 2-D tensor of `dtype` elements: dim0 innermost, row stride in bytes;
+// box0 x box1 elements per copy, with the given shared-memory swizzle.
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0,
+                    uint64_t dim1, uint64_t row_stride_bytes, uint32_t box0, uint32_t box1,
+                    CUtensorMapSwizzle swizzle);
+
 }  // namespace q4k

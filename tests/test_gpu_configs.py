@@ -71,15 +71,21 @@ def check_prefill(fields, x, rows, cols, rng, what, n_rows=96, n_tok=8):
     assert np.array_equal(host(d8), rd), f"{what}: q8 scales"
     assert np.array_equal(host(s), rs), f"{what}: q8 sums"
     y = host(q4k.q4k_gemm(w, rows, cols, q, d8, s))
+    # the binary16 form: same quants, and the tensor-copy GEMM on them
+    qh, dh, sh = q4k.q8_quantize_h16(torch.from_numpy(x).cuda())
+    assert np.array_equal(host(qh).astype(np.float32), rq.astype(np.float32)), f"{what}: h16 codes"
+    yh = host(q4k.q4k_gemm_h16(w, rows, cols, qh, dh, sh))
     tokens = x.shape[0]
     # sampled rows on sampled tokens, and every row on a few tokens
     trow = np.sort(rng.choice(tokens, 64, replace=False))
     sample = np.sort(rng.choice(rows, n_rows, replace=False))
     y_ref, norm = O.mmq(slice_rows(fields, sample), rq[trow], rd[trow], rs[trow])
     assert_close(y[np.ix_(trow, sample)], y_ref, norm, f"{what} rows sample")
+    assert_close(yh[np.ix_(trow, sample)], y_ref, norm, f"{what} rows sample (h16)")
     toks = np.sort(rng.choice(tokens, n_tok, replace=False))
     y_ref, norm = O.mmq(fields, rq[toks], rd[toks], rs[toks])
     assert_close(y[toks], y_ref, norm, f"{what} token sample")
+    assert_close(yh[toks], y_ref, norm, f"{what} token sample (h16)")
 
 
 def test_stack_prefill_2048_tokens():

@@ -196,6 +196,68 @@ def test_gemm_parity_and_block_dots(tokens, rows, cols):
     assert np.array_equal(p, O.block_dots(f["q"], rq))
 
 
+@pytest.mark.parametrize("case", ["adversarial", (3, 256), (512, 2560), (130, 9728)])
+def test_q8_quantize_h16_matches_the_int8_form(case):
+    """The binary16 quants hold exactly the int8 quants' values; d8 and the
+    sums are the same bits (and so equal to the oracle's)."""
+    x = adversarial_activations() if case == "adversarial" else synth.activations(*case, 301)
+    xd = torch.from_numpy(x).cuda()
+    q, d8, s = q4k.q8_quantize(xd)
+    qh, dh, sh = q4k.q8_quantize_h16(xd)
+    rq, rd, rs = O.quantize_q8_1(x)
+    assert np.array_equal(host(qh).astype(np.float32), rq.astype(np.float32))
+    assert np.array_equal(host(q), rq)
+    assert np.array_equal(host(dh).view(np.uint32), rd.view(np.uint32))
+    assert np.array_equal(host(sh), rs)
+
+
+@pytest.mark.parametrize("tokens,rows,cols", [
+    (1, 64, 256), (7, 70, 512), (16, 128, 256), (40, 64, 768), (64, 128, 2560),
+    (130, 200, 768), (33, 9, 4096), (200, 300, 1280), (129, 257, 512), (256, 384, 3328)])
+def test_gemm_h16_parity_and_block_dots(tokens, rows, cols):
+    f = synth.q4k_fields(rows, cols, [tokens, rows, cols, 16])
+    x = synth.activations(tokens, cols, [cols, tokens, 16])
+    w = pack_dev(f)
+    q, d8, s = q4k.q8_quantize_h16(torch.from_numpy(x).cuda())
+    y = host(q4k.q4k_gemm_h16(w, rows, cols, q, d8, s))
+    rq, rd, rs = O.quantize_q8_1(x)
+    y_ref, norm = O.mmq(f, rq, rd, rs)
+    assert_close(y, y_ref, norm, f"gemm_h16 {tokens}x{rows}x{cols}")
+    p = host(q4k.q4k_gemm_blockdots_h16(w, rows, cols, q))
+    assert np.array_equal(p, O.block_dots(f["q"], rq))
+
+
+def test_gemm_h16_block_dots_at_the_extremes():
+    rows, cols, tokens = 16, 512, 8
+    f = synth.q4k_fields(rows, cols, 90)
+    f["q"][:8] = 15
+    f["q"][8:, ::7] = 0
+    x = np.full((tokens, cols), 1.0, np.float32)
+    x[1:4:2] = -1.0
+    x[4:, ::5] *= -1.0
+    q, _, _ = q4k.q8_quantize_h16(torch.from_numpy(x).cuda())
+    p = host(q4k.q4k_gemm_blockdots_h16(pack_dev(f), rows, cols, q))
+    assert np.array_equal(p, O.block_dots(f["q"], O.quantize_q8_1(x)[0]))
+    assert p.max() == 15 * 127 * 32 and p.min() == -15 * 127 * 32
+
+
+def test_gemm_h16_equals_the_int8_entry_point():
+    """Same MMQ form, same q8_1 values: both entry points agree within the
+    bound of each against the oracle (they share no kernel code)."""
+    rows, cols, tokens = 300, 2560, 200
+    f = synth.q4k_fields(rows, cols, 3131)
+    x = synth.activations(tokens, cols, 3132)
+    w = pack_dev(f)
+    xd = torch.from_numpy(x).cuda()
+    y8 = host(q4k.q4k_gemm(w, rows, cols, *q4k.q8_quantize(xd)))
+    yh = host(q4k.q4k_gemm_h16(w, rows, cols, *q4k.q8_quantize_h16(xd)))
+    rq, rd, rs = O.quantize_q8_1(x)
+    y_ref, norm = O.mmq(f, rq, rd, rs)
+    assert_close(y8, y_ref, norm, "int8 entry")
+    assert_close(yh, y_ref, norm, "h16 entry")
+    assert_close(yh, y8.astype(np.float64), 2 * norm, "h16 vs int8")
+
+
 def test_gemm_block_dots_at_the_extremes():
     # rows 0-7 hold q = 15 everywhere and tokens 0-3 are all +1 or all -1, so
     # those block dots reach the extreme +-15*127*32; the rest are mixed.
@@ -213,15 +275,20 @@ def test_gemm_block_dots_at_the_extremes():
     assert p.max() == 15 * 127 * 32 and p.min() == -15 * 127 * 32
 
 
-def test_gemm_prefill_512_sampled():
+@pytest.mark.parametrize("form", ["int8", "h16"])
+def test_gemm_prefill_512_sampled(form):
     fields, xs = synth.prefill_4b_512()
     rng = np.random.default_rng(123)
     for name, inp in (("gate", "mlp_in"), ("down", "down_in")):
         f, x = fields[name], xs[inp]
         rows, cols = f["q"].shape
         w = pack_dev(f)
-        q, d8, s = quantize_dev(x)
-        y = host(q4k.q4k_gemm(w, rows, cols, q, d8, s))
+        if form == "int8":
+            q, d8, s = quantize_dev(x)
+            y = host(q4k.q4k_gemm(w, rows, cols, q, d8, s))
+        else:
+            q, d8, s = q4k.q8_quantize_h16(torch.from_numpy(x).cuda())
+            y = host(q4k.q4k_gemm_h16(w, rows, cols, q, d8, s))
         rq, rd, rs = O.quantize_q8_1(x)
         sample = np.sort(rng.choice(rows, 256, replace=False))
         y_ref, norm = O.mmq(slice_rows(f, sample), rq, rd, rs)

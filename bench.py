@@ -507,6 +507,31 @@ def run_ours(args, rank, world):
     token_engine = {f"batch{b}": stack_token(b, True) for b in (1, 4)}
     stack_indep = {f"batch{b}": stack_token(b, False) for b in (1, 4)}
 
+    def q8_layers(batch, n_layers=20):
+        """Decode layers at `batch` tokens through the q8_1 GEMV (MMQ form): per
+        layer q8_1 of the four inputs and one q4k_gemv_q8 launch per matrix."""
+        xs_b = {name: torch.from_numpy(synth.activations(batch, cols, [77, j, batch])).to(dev)
+                for j, (name, cols) in enumerate(synth.QWEN3_4B_INPUTS)}
+        q8b = {k: q4k.q8_quantize(v) for k, v in xs_b.items()}
+        ys_b = {n: torch.empty((batch, shape[n][0]), device=dev) for n in shape}
+
+        def run():
+            for L in range(n_layers):
+                layer = copies[L % n_copies]
+                for k, v in xs_b.items():
+                    q4k.q8_quantize(v, *q8b[k])
+                for n in shape:
+                    rows, cols, inp = shape[n]
+                    q4k.q4k_gemv_q8(layer[n], rows, cols, *q8b[inp], y=ys_b[n])
+        run()
+        torch.cuda.synchronize()
+        ms = time_graph(capture(run), 10) / n_layers
+        return {"us_per_layer": 1e3 * ms, "tokens_per_s_36_layers": batch / (36 * ms * 1e-3),
+                "GB/s": layer_bytes / (ms * 1e-3) / 1e9,
+                "note": "q8_1 of the 4 inputs + 7 q4k_gemv_q8 launches per layer, layers in sequence (graph)"}
+
+    q8_decode = {f"batch{b}": q8_layers(b) for b in (1, 4, 8)}
+
     # ---------------- single 2048x2048 GEMV, batch 1 (L2-resident: latency)
     f0, x0 = synth.single_gemv_2048(0)
     d0 = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev) for k, v in f0.items()}
@@ -694,6 +719,7 @@ def run_ours(args, rank, world):
             "layer_gemv_seq_with_waits": {"us_per_layer": 1e3 * ms_chain / args.steps,
                                           "GB/s": step_bytes * args.steps / (ms_chain * 1e-3) / 1e9},
             "token_36_layers_gemv_seq_with_waits": token_engine},
+        "decode_q8_1_gemv_per_layer": q8_decode,
         "decode_stack_36_layers_independent_jobs": {
             "note": "the 252 GEMVs of the stack with no dependencies between them (not a decode token)",
             **stack_indep},

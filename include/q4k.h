@@ -176,6 +176,25 @@ int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols,
              void* stream);
 
 /*
+ * q4k_gemv_q8 - the MMQ product for a few tokens as a GEMV: batch (1..8)
+ * rows of q8_1 activations against one weight matrix, in one weight pass
+ * (genie-ai-runtime §3: prompts of 18-33 tokens are the engine's prefill
+ * regime, far below a tensor-core tile; batched decode and speculative
+ * verification of a few tokens are the same shape).
+ *   y[b][o] = sum_blk ( d*sc * d8[b,blk] * P[b,o,blk] - dmin*m * d8[b,blk]*sum[b,blk] )
+ *             (+ residual[b][o] if residual != NULL),
+ *   P = exact integer dot of the 32 quants with the 32 int8 q8 values.
+ *   q8, d8, sum : q8_quantize() output for `batch` rows of width cols
+ *   y           : float [batch][rows]; residual as for q4k_gemv
+ * Accuracy as q4k_gemm (the bound at the top of this header, x = d8*q8).
+ * q4k_gemm and q4k_gemm_h16 use this kernel for up to 32 tokens (a launch
+ * per 8 tokens), and their block-dot exports then come from it.
+ */
+int q4k_gemv_q8(const void* w, int layout, int64_t rows, int64_t cols,
+                const int8_t* q8, const float* d8, const int32_t* sum,
+                int64_t batch, const float* residual, float* y, void* stream);
+
+/*
  * q4k_gemv_multi - one decode GEMV launch over n (1..4) matrices that share
  * the input x (genie-ai-runtime §4, Path C: one kernel for the QKV triple and
  * for the gate/up pair).  w, rows, y (and residual, if not NULL) are HOST

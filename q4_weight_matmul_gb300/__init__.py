@@ -44,6 +44,7 @@ SIGNATURES = {
     "q8_quantize": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q8_quantize_h16": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q4k_gemv": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "q4k_gemv_q8": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P, _P]),
     "q4k_gemv_multi": (_I, [_I, _P, _I, _P, _I64, _P, _I64, _P, _P, _P]),
     "q4k_gemv_seq_workspace_bytes": (ctypes.c_size_t, [_P, _I, _I64]),
     "q4k_gemv_seq": (_I, [_P, _I, _I, _I64, _P, ctypes.c_size_t, _P]),
@@ -195,6 +196,19 @@ def q4k_gemv(w, rows: int, cols: int, x, residual=None, y=None, layout: int = BL
                           _ptr(x, torch.float32, "x"), batch,
                           _ptr(residual, torch.float32, "residual"),
                           _ptr(y, torch.float32, "y"), _stream(stream)), "q4k_gemv")
+    return y
+
+
+def q4k_gemv_q8(w, rows: int, cols: int, q8, d8, s, residual=None, y=None, layout: int = BLOCK144, stream=None):
+    """MMQ GEMV over q8_1 activations (``q8_quantize`` output, 1..8 rows):
+    ``y[b] = W x_hat[b] (+ residual[b])``."""
+    batch = q8.shape[0]
+    if y is None:
+        y = torch.empty((batch, rows), dtype=torch.float32, device=q8.device)
+    _check(lib().q4k_gemv_q8(_ptr(w, torch.uint8, "w"), layout, rows, cols, _ptr(q8, torch.int8, "q8"),
+                             _ptr(d8, torch.float32, "d8"), _ptr(s, torch.int32, "sum"), batch,
+                             _ptr(residual, torch.float32, "residual"), _ptr(y, torch.float32, "y"),
+                             _stream(stream)), "q4k_gemv_q8")
     return y
 
 
@@ -351,6 +365,7 @@ def q4k_version() -> str:
 
 
 __all__ = ["build", "lib", "Q4KError", "BLOCK144", "LAYOUT_GPU", "q4k_packed_bytes", "q4k_pack", "q4k_unpack",
+           "q4k_gemv_q8",
            "q8_1_bytes", "q8_quantize", "q8_quantize_h16", "q4k_gemm_h16", "q4k_gemm_blockdots_h16",
            "q4k_gemv", "q4k_gemv_multi", "GemvJob", "GemvSeq", "q4k_gemv_seq", "q4k_gemv_seq_static", "q4k_gemm",
            "q4k_gemm_blockdots", "q4k_device_error",

@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 #include <q4k.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -224,6 +225,23 @@ int q4k_gemv_multi(int n, const void* const* w, int layout, const int64_t* rows,
   return e == cudaSuccess ? Q4K_OK : record_cuda(e);
 }
 
+int q4k_gemv_q8(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8, const float* d8,
+                const int32_t* sum, int64_t batch, const float* residual, float* y, void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_layout(layout)) return e;
+  if (batch < 0 || batch > 8) return batch < 0 ? Q4K_ERR_INVALID_ARG : Q4K_ERR_UNSUPPORTED;
+  if (rows == 0 || batch == 0) return Q4K_OK;
+  if (!w || !q8 || !d8 || !sum || !y) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(q8) || !aligned16(d8) || !aligned16(sum) || !aligned16(y) ||
+      (residual && !aligned16(residual)))
+    return Q4K_ERR_ALIGNMENT;
+  if (!gemv_q8_supported(rows, cols, (int)batch)) return Q4K_ERR_UNSUPPORTED;
+  cudaError_t e = launch_gemv_q8_block144(static_cast<const uint8_t*>(w), rows, cols, q8, false, d8, sum,
+                                          (int)batch, residual, y, nullptr, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
 int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols, const float* x,
              int64_t batch, const float* residual, float* y, void* stream) {
   if (int e = check_rows(rows)) return e;
@@ -260,6 +278,27 @@ static int check_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t b
   return Q4K_OK;
 }
 
+// Token counts up to this go through the q8_1 GEMV (one weight pass per 8
+// tokens) instead of a 128-token tensor-core tile.
+constexpr int64_t kGemvTokens = 32;
+
+// The MMQ product for a few tokens: q8_1 GEMV launches of up to 8 tokens.
+static cudaError_t gemm_by_gemv(const uint8_t* w, int64_t rows, int64_t cols, const void* q8, bool h16,
+                                const float* d8, const int32_t* sum, int64_t tokens, float* y, int32_t* p,
+                                cudaStream_t s) {
+  const int64_t nsub = cols / kSub;
+  for (int64_t t0 = 0; t0 < tokens; t0 += 8) {
+    const int n = (int)std::min<int64_t>(8, tokens - t0);
+    const void* qt = h16 ? static_cast<const void*>(static_cast<const uint16_t*>(q8) + t0 * cols)
+                         : static_cast<const void*>(static_cast<const int8_t*>(q8) + t0 * cols);
+    cudaError_t e = launch_gemv_q8_block144(w, rows, cols, qt, h16, d8 ? d8 + t0 * nsub : nullptr,
+                                            sum ? sum + t0 * nsub : nullptr, n, nullptr,
+                                            y ? y + t0 * rows : nullptr, p ? p + t0 * rows * nsub : nullptr, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 static int gemm_common(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8,
                        const float* d8, const int32_t* sum, int64_t tokens, float* y,
                        int32_t* p, void* stream) {
@@ -274,14 +313,15 @@ static int gemm_common(const void* w, int layout, int64_t rows, int64_t cols, co
       (y && !aligned16(y)) || (p && !aligned16(p)))
     return Q4K_ERR_ALIGNMENT;
   cudaError_t e;
-  if (gemm_tc_supported(tokens)) {
+  if (tokens <= kGemvTokens) {
+    if (!gemv_q8_supported(rows, cols, (int)std::min<int64_t>(tokens, 8))) return Q4K_ERR_UNSUPPORTED;
+    e = gemm_by_gemv(static_cast<const uint8_t*>(w), rows, cols, q8, false, d8, sum, tokens, y, p,
+                     static_cast<cudaStream_t>(stream));
+  } else {
     int* err = device_error_word();
     if (!err) return record_cuda(cudaGetLastError());
     e = launch_gemm_block144(static_cast<const uint8_t*>(w), rows, cols, q8, d8, sum, tokens, y, p,
                              err, static_cast<cudaStream_t>(stream));
-  } else {
-    e = launch_gemm_dp4a(static_cast<const uint8_t*>(w), rows, cols, q8, d8, sum, tokens, y, p,
-                         static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? Q4K_OK : record_cuda(e);
 }
@@ -310,10 +350,17 @@ static int gemm_h16_common(const void* w, int layout, int64_t rows, int64_t cols
   if (!aligned16(w) || !aligned16(q16) || (d8 && !aligned16(d8)) || (sum && !aligned16(sum)) ||
       (y && !aligned16(y)) || (p && !aligned16(p)))
     return Q4K_ERR_ALIGNMENT;
-  int* err = device_error_word();
-  if (!err) return record_cuda(cudaGetLastError());
-  cudaError_t e = launch_gemm_h16(static_cast<const uint8_t*>(w), rows, cols, q16, d8, sum, tokens, y, p, err,
-                                  static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (tokens <= kGemvTokens) {
+    if (!gemv_q8_supported(rows, cols, (int)std::min<int64_t>(tokens, 8))) return Q4K_ERR_UNSUPPORTED;
+    e = gemm_by_gemv(static_cast<const uint8_t*>(w), rows, cols, q16, true, d8, sum, tokens, y, p,
+                     static_cast<cudaStream_t>(stream));
+  } else {
+    int* err = device_error_word();
+    if (!err) return record_cuda(cudaGetLastError());
+    e = launch_gemm_h16(static_cast<const uint8_t*>(w), rows, cols, q16, d8, sum, tokens, y, p, err,
+                        static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? Q4K_OK : record_cuda(e);
 }
 

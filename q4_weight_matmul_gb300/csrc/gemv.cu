@@ -29,6 +29,10 @@
 //
 // Arithmetic: 32-bit fixed-point activation digit planes and exact integer
 // dp4a block sums, scales applied in fp32 (gemv_common.cuh).
+//
+// q8_1 activations (q4k_gemv_q8, and q4k_gemm for a few tokens): the same
+// kernel with the activation kind a template parameter; the quants are
+// staged as one int8 plane and the block dots are the exact integer MMQ dots.
 #include "gemv_common.cuh"
 #include "q4k_internal.h"
 #include "tc_ptx.cuh"
@@ -64,8 +68,17 @@ struct GemvParams {
   int pdl;                      // launched as a programmatic dependent
   int trigger_late;             // launch dependents after the units, not at start
   const float* x;
+  const void* xq;               // q8_1 quants (int8, or binary16 integers)
+  const float* d8;
+  const int32_t* qsum;
+  int32_t* p_out;               // non-null: store the q8 block dots too (one matrix)
   int* err;
 };
+
+// activation kinds
+constexpr int kActF32 = 0;      // fp32 x, fixed-point digit planes
+constexpr int kActQ8 = 1;       // q8_1, int8 quants
+constexpr int kActQ8H = 2;      // q8_1, binary16 quants
 
 __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
@@ -75,11 +88,11 @@ struct Layout {
   size_t xs, xsum, part, stages, bars, total;
 };
 
-__host__ __device__ inline Layout layout(int B, int nb, int ring, int part_floats) {
+__host__ __device__ inline Layout layout(int B, int nb, int ring, int part_floats, bool q8) {
   Layout L;
   L.xs = 0;
-  L.xsum = L.xs + gemv::xs_bytes(B, nb);
-  L.part = L.xsum + gemv::xss_bytes(B, nb);
+  L.xsum = L.xs + (q8 ? gemv::xq8_bytes(B, nb) : gemv::xs_bytes(B, nb));
+  L.part = L.xsum + (q8 ? gemv::xq8s_bytes(B, nb) : gemv::xss_bytes(B, nb));
   L.stages = (L.part + sizeof(float) * (size_t)part_floats + 1023) & ~size_t(1023);
   L.bars = L.stages + (size_t)ring * kStageBytes;
   L.total = L.bars + sizeof(uint64_t) * 2 * ring + 16 + 1024;   // + issue counter, + slack to align the base
@@ -95,8 +108,9 @@ __device__ __forceinline__ int mat_of(const GemvParams& P, int g) {
   return m;
 }
 
-// LPR: lanes per row (1, 2 or 4); RB = 32 / LPR rows per block.
-template <int B, int LPR>
+// LPR: lanes per row (1, 2 or 4); RB = 32 / LPR rows per block.  ACT: the
+// activation kind.
+template <int B, int LPR, int ACT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
     const __grid_constant__ GemvParams P) {
   constexpr int RB = 32 / LPR;              // rows per block
@@ -112,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
   const int my_rb = max(0, min(P.rb_per_cta, n_rb - rb0));
   const int n_sj = (nb + SB - 1) / SB;      // stages per row block
   const int n_stages = my_rb * n_sj;
-  const Layout L = layout(B, nb, ring, B * rb_pass * nb * RB);
+  const Layout L = layout(B, nb, ring, B * rb_pass * nb * RB, ACT != kActF32);
   uint8_t* xs = smem + L.xs;
   float2* xss = reinterpret_cast<float2*>(smem + L.xsum);
   float* part = reinterpret_cast<float*>(smem + L.part);      // [B][rb of the pass][nb][RB]
@@ -174,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
 
   // -------------------------------------------------------------- consumers
   if (P.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
-  gemv::stage_x<B, kConsumers, false>(P.x, nb, xs, xss, tid);
+  if constexpr (ACT == kActF32) gemv::stage_x<B, kConsumers, false>(P.x, nb, xs, xss, tid);
+  else gemv::stage_q8<B, kConsumers, ACT == kActQ8H>(P.xq, P.d8, P.qsum, nb, xs, xss, tid);
   named_sync_consumers();
   const gemv::XView xv = gemv::make_view(xs, xss, P.x, B, nb);
 
@@ -215,7 +230,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
       if (sb < nb) {
         // stage laid out [SB][RB][144] (rows inner)
         const uint8_t* p = stages + (size_t)slot * kStageBytes + ((size_t)z * RB + r_in) * kBlockBytes;
-        gemv::superblock_dot<B, CPL, false>(p, xv, sb, c0, acc);
+        if constexpr (ACT == kActF32) {
+          gemv::superblock_dot<B, CPL, false>(p, xv, sb, c0, acc);
+        } else {
+          int32_t* pout = nullptr;
+          if (P.p_out) {
+            const int g = rb0 + pb + rbl;
+            const int row = (g - P.rb_start[0]) * RB + r_in;
+            if (row < P.rows[0]) pout = P.p_out + ((size_t)row * nb + sb) * 8;
+          }
+          gemv::superblock_dot_q8<B, CPL>(p, xs, xss, nb, sb, c0, acc, pout, (size_t)P.rows[0] * nb * 8);
+        }
       }
       // release the stage once every lane of the warp has read it
       __syncwarp();
@@ -239,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
       const int m = mat_of(P, g);
       const int rows = P.rows[m];
       const int row = (g - P.rb_start[m]) * RB + r;
-      if (row < rows && ok) {
+      if (row < rows && ok && P.y[m]) {   // (no y when only the block dots are wanted)
         const float* pp = part + (((size_t)b * rb_pass + rbl) * nb) * RB + r;
         float v = 0.0f;
         for (int s2 = 0; s2 < nb; ++s2) v += pp[(size_t)s2 * RB];
@@ -270,7 +295,7 @@ struct Plan {
   size_t smem;
 };
 
-Plan make_plan(int B, const int64_t* rows, int n_mats, int nb, const DeviceInfo& info) {
+Plan make_plan(int B, const int64_t* rows, int n_mats, int nb, const DeviceInfo& info, bool q8) {
   Plan p{};
   // rows per block: the one whose busiest SM holds the fewest rows (ties go to
   // the taller block, which decodes scales less often)
@@ -299,7 +324,7 @@ Plan make_plan(int B, const int64_t* rows, int n_mats, int nb, const DeviceInfo&
   const size_t caps[2] = {kPairSmem, (size_t)info.max_smem_optin};
   for (size_t cap : caps) {
     for (int ring = kMaxRing; ring >= 2 && p.ring == 0; --ring) {
-      const size_t total = layout(B, nb, ring, B * p.rb_pass * nb * RB).total;
+      const size_t total = layout(B, nb, ring, B * p.rb_pass * nb * RB, q8).total;
       if (total <= cap) {
         p.ring = ring;
         p.smem = total;
@@ -310,13 +335,13 @@ Plan make_plan(int B, const int64_t* rows, int n_mats, int nb, const DeviceInfo&
   return p;
 }
 
-template <int B, int LPR>
+template <int B, int LPR, int ACT>
 cudaError_t launch_bl(const GemvParams& params, const Plan& p, int dev, const DeviceInfo& info,
                       cudaStream_t s) {
   static int s_limit[64];
   int& limit = s_limit[dev & 63];
   if (limit < info.max_smem_optin) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_block144_kernel<B, LPR>,
+    cudaError_t e = cudaFuncSetAttribute(gemv_block144_kernel<B, LPR, ACT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          info.max_smem_optin);
     if (e != cudaSuccess) return e;
@@ -332,16 +357,25 @@ cudaError_t launch_bl(const GemvParams& params, const Plan& p, int dev, const De
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_mode() != 0 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemv_block144_kernel<B, LPR>, params);
+  return cudaLaunchKernelEx(&cfg, gemv_block144_kernel<B, LPR, ACT>, params);
 }
 
+struct ActIn {   // the activations of one launch
+  int kind;
+  const float* x;
+  const void* xq;
+  const float* d8;
+  const int32_t* qsum;
+  int32_t* p_out;
+};
+
 template <int B>
-cudaError_t launch_b(const uint8_t* const* w, const int64_t* rows, int n_mats, int nb, const float* x,
+cudaError_t launch_b(const uint8_t* const* w, const int64_t* rows, int n_mats, int nb, const ActIn& act,
                      const float* const* residual, float* const* y, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   const DeviceInfo& info = device_info(dev);
-  const Plan p = make_plan(B, rows, n_mats, nb, info);
+  const Plan p = make_plan(B, rows, n_mats, nb, info, act.kind != kActF32);
   if (p.ring == 0) return cudaErrorNotSupported;
   GemvParams params;
   memset(&params, 0, sizeof(params));
@@ -368,11 +402,36 @@ cudaError_t launch_b(const uint8_t* const* w, const int64_t* rows, int n_mats, i
   params.ring = p.ring;
   params.pdl = pdl_mode() != 0 ? 1 : 0;
   params.trigger_late = pdl_mode() == 2 ? 1 : 0;
-  params.x = x;
-  switch (p.lpr) {
-    case 1: return launch_bl<B, 1>(params, p, dev, info, s);
-    case 2: return launch_bl<B, 2>(params, p, dev, info, s);
-    default: return launch_bl<B, 4>(params, p, dev, info, s);
+  params.x = act.x;
+  params.xq = act.xq;
+  params.d8 = act.d8;
+  params.qsum = act.qsum;
+  params.p_out = act.p_out;
+  switch (act.kind * 4 + p.lpr) {
+    case kActF32 * 4 + 1: return launch_bl<B, 1, kActF32>(params, p, dev, info, s);
+    case kActF32 * 4 + 2: return launch_bl<B, 2, kActF32>(params, p, dev, info, s);
+    case kActF32 * 4 + 4: return launch_bl<B, 4, kActF32>(params, p, dev, info, s);
+    case kActQ8 * 4 + 1: return launch_bl<B, 1, kActQ8>(params, p, dev, info, s);
+    case kActQ8 * 4 + 2: return launch_bl<B, 2, kActQ8>(params, p, dev, info, s);
+    case kActQ8 * 4 + 4: return launch_bl<B, 4, kActQ8>(params, p, dev, info, s);
+    case kActQ8H * 4 + 1: return launch_bl<B, 1, kActQ8H>(params, p, dev, info, s);
+    case kActQ8H * 4 + 2: return launch_bl<B, 2, kActQ8H>(params, p, dev, info, s);
+    default: return launch_bl<B, 4, kActQ8H>(params, p, dev, info, s);
+  }
+}
+
+cudaError_t launch_batch(const uint8_t* const* w, const int64_t* rows, int n_mats, int nb, int batch,
+                         const ActIn& act, const float* const* residual, float* const* y, cudaStream_t s) {
+  switch (batch) {
+    case 1: return launch_b<1>(w, rows, n_mats, nb, act, residual, y, s);
+    case 2: return launch_b<2>(w, rows, n_mats, nb, act, residual, y, s);
+    case 3: return launch_b<3>(w, rows, n_mats, nb, act, residual, y, s);
+    case 4: return launch_b<4>(w, rows, n_mats, nb, act, residual, y, s);
+    case 5: return launch_b<5>(w, rows, n_mats, nb, act, residual, y, s);
+    case 6: return launch_b<6>(w, rows, n_mats, nb, act, residual, y, s);
+    case 7: return launch_b<7>(w, rows, n_mats, nb, act, residual, y, s);
+    case 8: return launch_b<8>(w, rows, n_mats, nb, act, residual, y, s);
+    default: return cudaErrorNotSupported;
   }
 }
 
@@ -384,24 +443,32 @@ bool gemv_supported(const int64_t* rows, int n_mats, int64_t cols, int batch) {
   if (batch < 1 || batch > 8 || n_mats < 1 || n_mats > kMaxMats) return false;
   int dev = 0;
   cudaGetDevice(&dev);
-  return make_plan(batch, rows, n_mats, (int)(cols / kQK), device_info(dev)).ring != 0;
+  return make_plan(batch, rows, n_mats, (int)(cols / kQK), device_info(dev), false).ring != 0;
+}
+
+bool gemv_q8_supported(int64_t rows, int64_t cols, int batch) {
+  if (batch < 1 || batch > 8) return false;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return make_plan(batch, &rows, 1, (int)(cols / kQK), device_info(dev), true).ring != 0;
+}
+
+cudaError_t launch_gemv_q8_block144(const uint8_t* w, int64_t rows, int64_t cols, const void* q8, bool h16,
+                                    const float* d8, const int32_t* sum, int batch, const float* residual,
+                                    float* y, int32_t* p_out, cudaStream_t s) {
+  ActIn act{h16 ? kActQ8H : kActQ8, nullptr, q8, d8, sum, p_out};
+  const uint8_t* const ws[1] = {w};
+  const float* const res[1] = {residual};
+  float* const ys[1] = {y};
+  return launch_batch(ws, &rows, 1, (int)(cols / kQK), batch, act, res, ys, s);
 }
 
 cudaError_t launch_gemv_block144(const uint8_t* const* w, const int64_t* rows, int n_mats, int64_t cols,
                                  const float* x, int batch, const float* const* residual,
                                  float* const* y, cudaStream_t s) {
   const int nb = (int)(cols / kQK);
-  switch (batch) {
-    case 1: return launch_b<1>(w, rows, n_mats, nb, x, residual, y, s);
-    case 2: return launch_b<2>(w, rows, n_mats, nb, x, residual, y, s);
-    case 3: return launch_b<3>(w, rows, n_mats, nb, x, residual, y, s);
-    case 4: return launch_b<4>(w, rows, n_mats, nb, x, residual, y, s);
-    case 5: return launch_b<5>(w, rows, n_mats, nb, x, residual, y, s);
-    case 6: return launch_b<6>(w, rows, n_mats, nb, x, residual, y, s);
-    case 7: return launch_b<7>(w, rows, n_mats, nb, x, residual, y, s);
-    case 8: return launch_b<8>(w, rows, n_mats, nb, x, residual, y, s);
-    default: return cudaErrorNotSupported;
-  }
+  ActIn act{kActF32, x, nullptr, nullptr, nullptr, nullptr};
+  return launch_batch(w, rows, n_mats, nb, batch, act, residual, y, s);
 }
 
 }  // namespace q4k

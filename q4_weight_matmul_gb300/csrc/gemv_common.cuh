@@ -400,5 +400,119 @@ __device__ __forceinline__ void superblock_dot(const uint8_t* p, const XView& X,
   }
 }
 
+// ---------------------------------------------------------------------------
+// q8_1 activations (the MMQ form for a few tokens).  The int8 quants of one
+// (token, superblock, chunk) take one 64-byte region laid out like a digit
+// plane: 16-byte words at (h*2 + s)*16, word k holding positions
+// 16h+4k..+3 of sub-block 2c+s.  Per sub-block: (d8, d8*S) as a float2.
+constexpr int kRegionQ8 = 64;
+__host__ __device__ constexpr size_t xq8_bytes(int B, int nb) { return (size_t)B * nb * 4 * kRegionQ8; }
+__host__ __device__ constexpr size_t xq8s_bytes(int B, int nb) { return sizeof(float2) * (size_t)B * nb * 8; }
+
+// Stage q8 [B][nb*256] (int8, or binary16 integers when kH16), d8 and the
+// block sums once per CTA.  One thread takes 16 quants (half a sub-block).
+template <int B, int NT, bool kH16>
+__device__ __forceinline__ void stage_q8(const void* __restrict__ q8, const float* __restrict__ d8,
+                                         const int32_t* __restrict__ ssum, int nb, uint8_t* xs, float2* xss,
+                                         int tid) {
+  const int n16 = B * nb * 16;   // halves of sub-blocks
+  for (int i = tid; i < n16; i += NT) {
+    const int b = i / (nb * 16), rem = i - b * nb * 16;
+    const int sb = rem >> 4, j = (rem >> 1) & 7, h = rem & 1;
+    const int c = j >> 1, sf = j & 1;
+    const size_t e0 = ((size_t)b * nb + sb) * 256 + 32 * j + 16 * h;   // first element
+    uint4 w;
+    if (kH16) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q8) + e0);
+      const uint4 a = __ldg(src), bq = __ldg(src + 1);
+      const uint32_t hw[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+      uint32_t out[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __half2 lo = *reinterpret_cast<const __half2*>(&hw[2 * k]);
+        const __half2 hi = *reinterpret_cast<const __half2*>(&hw[2 * k + 1]);
+        const int v0 = __half2int_rn(__low2half(lo)), v1 = __half2int_rn(__high2half(lo));
+        const int v2 = __half2int_rn(__low2half(hi)), v3 = __half2int_rn(__high2half(hi));
+        out[k] = (uint32_t)(v0 & 0xFF) | ((uint32_t)(v1 & 0xFF) << 8) | ((uint32_t)(v2 & 0xFF) << 16) |
+                 ((uint32_t)(v3 & 0xFF) << 24);
+      }
+      w = make_uint4(out[0], out[1], out[2], out[3]);
+    } else {
+      w = __ldg(reinterpret_cast<const uint4*>(static_cast<const int8_t*>(q8) + e0));
+    }
+    *reinterpret_cast<uint4*>(xs + (((size_t)b * nb + sb) * 4 + c) * kRegionQ8 + (h * 2 + sf) * 16) = w;
+    if (h == 0) {   // (scales are absent when only the block dots are wanted)
+      const size_t sbk = ((size_t)b * nb + sb) * 8 + j;
+      const float dd = d8 ? __ldg(d8 + sbk) : 0.0f;
+      xss[sbk] = make_float2(dd, ssum ? dd * (float)__ldg(ssum + sbk) : 0.0f);
+    }
+  }
+}
+
+// superblock_dot for q8 activations: per sub-block the exact integer
+// P = sum q*q8 (dp4a, |P| <= 15*127*32), then
+//     acc += d*sc_j*d8_j*P_j - dmin*m_j*(d8_j*S_j).
+// With `pout` (test export) each P_j is stored at pout[b * pstride + j]
+// (the lane's sub-blocks only).
+template <int B, int CPL>
+__device__ __forceinline__ void superblock_dot_q8(const uint8_t* p, const uint8_t* xs, const float2* xss, int nb,
+                                                  int sb, int c0, float (&acc)[B], int32_t* pout, size_t pstride) {
+  const uint4 hd = *reinterpret_cast<const uint4*>(p);
+  const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
+  const uint32_t sc03 = hd.y & 0x3F3F3F3Fu, m03 = hd.z & 0x3F3F3F3Fu;
+  const uint32_t sc47 = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+  const uint32_t m47 = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+  float scaled[B], mins[B];
+#pragma unroll
+  for (int b = 0; b < B; ++b) scaled[b] = mins[b] = 0.0f;
+#pragma unroll
+  for (int cc = 0; cc < CPL; ++cc) {
+    const int c = c0 + cc;
+    const uint4 q0 = *reinterpret_cast<const uint4*>(p + 16 + 32 * c);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(p + 32 + 32 * c);
+    int lo[B], hi[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) lo[b] = hi[b] = 0;
+    const uint8_t* xc0 = xs + ((size_t)sb * 4 + c) * kRegionQ8;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 qq = h ? q1 : q0;
+      uint32_t ql[4], qh[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w = word_of(qq, k);
+        ql[k] = w & 0x0F0F0F0Fu;
+        qh[k] = (w >> 4) & 0x0F0F0F0Fu;
+      }
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const uint4* xp = reinterpret_cast<const uint4*>(xc0 + (size_t)b * nb * 4 * kRegionQ8) + h * 2;
+        const uint4 xl = xp[0], xh = xp[1];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          lo[b] = dp4a_us(ql[k], word_of(xl, k), lo[b]);
+          hi[b] = dp4a_us(qh[k], word_of(xh, k), hi[b]);
+        }
+      }
+    }
+    const uint32_t scw = c < 2 ? sc03 : sc47, mw = c < 2 ? m03 : m47;
+    const int bi = 2 * (c & 1);
+    const float sc_lo = byte_f(scw, bi), sc_hi = byte_f(scw, bi + 1);
+    const float m_lo = byte_f(mw, bi), m_hi = byte_f(mw, bi + 1);
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const float4 ss = *reinterpret_cast<const float4*>(xss + ((size_t)b * nb + sb) * 8 + 2 * c);
+      scaled[b] = fmaf(sc_hi * ss.z, (float)hi[b], fmaf(sc_lo * ss.x, (float)lo[b], scaled[b]));
+      mins[b] = fmaf(m_hi, ss.w, fmaf(m_lo, ss.y, mins[b]));
+      if (pout) {
+        pout[(size_t)b * pstride + 2 * c] = lo[b];
+        pout[(size_t)b * pstride + 2 * c + 1] = hi[b];
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < B; ++b) acc[b] = fmaf(dm.x, scaled[b], -dm.y * mins[b]);
+}
+
 }  // namespace gemv
 }  // namespace q4k

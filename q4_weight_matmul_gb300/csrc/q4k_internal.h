@@ -49,6 +49,13 @@ cudaError_t launch_gemv_block144(const uint8_t* const* w, const int64_t* rows, i
                                  const float* x, int batch, const float* const* residual,
                                  float* const* y, cudaStream_t s);
 bool gemv_supported(const int64_t* rows, int n_mats, int64_t cols, int batch);
+// The same kernel over q8_1 activations (batch 1..8 tokens), int8 quants or
+// (h16) binary16 integers; p_out (nullable) receives the exact block dots
+// [batch][rows][cols/32].
+bool gemv_q8_supported(int64_t rows, int64_t cols, int batch);
+cudaError_t launch_gemv_q8_block144(const uint8_t* w, int64_t rows, int64_t cols, const void* q8, bool h16,
+                                    const float* d8, const int32_t* sum, int batch, const float* residual,
+                                    float* y, int32_t* p_out, cudaStream_t s);
 
 // Persistent GEMV over an ordered job list (q4k_gemv_seq).  Both return a
 // q4k_status; launch_gemv_seq stores the launch's CUDA error in *cuda_err.
@@ -65,13 +72,6 @@ int gemv_seq_launch(const void* plan, cudaStream_t s, cudaError_t* cuda_err);
 // The same with the library's built-in scratch array as the workspace.
 int launch_gemv_seq_static(const q4k_gemv_job* jobs, int n_jobs, int batch, cudaStream_t s,
                            cudaError_t* cuda_err);
-
-// Small-tile integer MMQ on CUDA cores (dp4a).  When `p_out` is non-null
-// the kernel stores the raw per-block integer dots there instead of y.
-cudaError_t launch_gemm_dp4a(const uint8_t* w, int64_t rows, int64_t cols,
-                             const int8_t* q8, const float* d8,
-                             const int32_t* sum, int64_t tokens, float* y,
-                             int32_t* p_out, cudaStream_t s);
 
 // Tensor-core prefill MMQ GEMM (tcgen05).  When `p_out` is non-null the
 // kernel stores the raw per-block integer dots there instead of y (test

@@ -2,6 +2,7 @@
 
     python -m q4_weight_matmul_gb300.profile_case gemv --rows 9728 --cols 2560 --batch 1 --reps 5
     python -m q4_weight_matmul_gb300.profile_case gemm --rows 9728 --cols 2560 --tokens 512
+    python -m q4_weight_matmul_gb300.profile_case gemm_h16 --rows 9728 --cols 2560 --tokens 512
     python -m q4_weight_matmul_gb300.profile_case q8 --tokens 512 --cols 9728
     python -m q4_weight_matmul_gb300.profile_case pack --rows 9728 --cols 2560
     python -m q4_weight_matmul_gb300.profile_case seq --layers 13 --batch 1 --reps 3
@@ -57,7 +58,7 @@ def run_seq(a, dev, gen):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["gemv", "gemm", "q8", "pack", "seq"])
+    ap.add_argument("kernel", choices=["gemv", "gemm", "gemm_h16", "q8", "pack", "seq"])
     ap.add_argument("--layers", type=int, default=13)
     ap.add_argument("--rows", type=int, default=9728)
     ap.add_argument("--cols", type=int, default=2560)
@@ -75,7 +76,7 @@ def main():
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
     f = rand_fields(a.rows, a.cols, dev, gen)
     w0 = q4k.q4k_pack(*f)
-    n = max(1, math.ceil(2 * l2 / w0.numel())) if a.kernel in ("gemv", "gemm") else 1
+    n = max(1, math.ceil(2 * l2 / w0.numel())) if a.kernel in ("gemv", "gemm", "gemm_h16") else 1
     ws = [w0] + [w0.clone() for _ in range(n - 1)]
     if a.kernel == "gemv":
         x = torch.randn((a.batch, a.cols), device=dev, generator=gen)
@@ -88,6 +89,12 @@ def main():
         y = torch.empty((a.tokens, a.rows), device=dev)
         for i in range(a.reps):
             q4k.q4k_gemm(ws[i % n], a.rows, a.cols, q, d8, s, y=y)
+    elif a.kernel == "gemm_h16":
+        x = torch.randn((a.tokens, a.cols), device=dev, generator=gen)
+        q, d8, s = q4k.q8_quantize_h16(x)
+        y = torch.empty((a.tokens, a.rows), device=dev)
+        for i in range(a.reps):
+            q4k.q4k_gemm_h16(ws[i % n], a.rows, a.cols, q, d8, s, y=y)
     elif a.kernel == "q8":
         x = torch.randn((a.tokens, a.cols), device=dev, generator=gen)
         out = q4k.q8_quantize(x)

@@ -179,7 +179,7 @@ def quantize_dev(x):
     return q, d8, s
 
 
-# token counts below 16 run the dp4a kernel, the rest the tensor-core kernel
+# token counts up to 32 run the q8_1 GEMV, the rest the tensor-core kernel
 @pytest.mark.parametrize("tokens,rows,cols", [
     (1, 64, 256), (5, 70, 512), (15, 33, 768), (16, 128, 256), (40, 64, 256), (64, 128, 2560),
     (130, 200, 768), (33, 9, 4096), (200, 300, 1280), (129, 257, 512)])
@@ -227,8 +227,9 @@ def test_gemm_h16_parity_and_block_dots(tokens, rows, cols):
     assert np.array_equal(p, O.block_dots(f["q"], rq))
 
 
-def test_gemm_h16_block_dots_at_the_extremes():
-    rows, cols, tokens = 16, 512, 8
+@pytest.mark.parametrize("tokens", [8, 48])
+def test_gemm_h16_block_dots_at_the_extremes(tokens):
+    rows, cols = 16, 512
     f = synth.q4k_fields(rows, cols, 90)
     f["q"][:8] = 15
     f["q"][8:, ::7] = 0
@@ -258,10 +259,49 @@ def test_gemm_h16_equals_the_int8_entry_point():
     assert_close(yh, y8.astype(np.float64), 2 * norm, "h16 vs int8")
 
 
-def test_gemm_block_dots_at_the_extremes():
+@pytest.mark.parametrize("batch,rows,cols", [(1, 96, 256), (2, 100, 768), (4, 257, 2560), (8, 1000, 4096),
+                                             (5, 33, 9728)])
+def test_gemv_q8_parity(batch, rows, cols):
+    """The few-token MMQ as a GEMV, with and without a residual."""
+    f = synth.q4k_fields(rows, cols, [batch, rows, cols, 8])
+    x = synth.activations(batch, cols, [cols, batch, 8])
+    r = synth.residual(batch, rows, [rows, batch, 8])
+    w = pack_dev(f)
+    q, d8, s = quantize_dev(x)
+    rq, rd, rs = O.quantize_q8_1(x)
+    y_ref, norm = O.mmq(f, rq, rd, rs)
+    y = host(q4k.q4k_gemv_q8(w, rows, cols, q, d8, s))
+    assert_close(y, y_ref, norm, f"gemv_q8 {batch}x{rows}x{cols}")
+    yr = host(q4k.q4k_gemv_q8(w, rows, cols, q, d8, s, residual=torch.from_numpy(r).cuda()))
+    assert_close(yr, y_ref + r, norm + np.abs(r.astype(np.float64)), f"gemv_q8 {batch}x{rows}x{cols} + residual")
+
+
+@pytest.mark.parametrize("tokens", [3, 8, 9, 32])
+def test_few_token_gemm_runs_the_gemv_and_its_dots_are_exact(tokens):
+    """q4k_gemm / q4k_gemm_h16 with up to 32 tokens go through the q8_1 GEMV
+    (a launch per 8 tokens); outputs within the bound, block dots bit-exact."""
+    rows, cols = 300, 2560
+    f = synth.q4k_fields(rows, cols, [tokens, 31])
+    x = synth.activations(tokens, cols, [tokens, 32])
+    w = pack_dev(f)
+    xd = torch.from_numpy(x).cuda()
+    rq, rd, rs = O.quantize_q8_1(x)
+    y_ref, norm = O.mmq(f, rq, rd, rs)
+    q, d8, s = q4k.q8_quantize(xd)
+    qh, dh, sh = q4k.q8_quantize_h16(xd)
+    assert_close(host(q4k.q4k_gemm(w, rows, cols, q, d8, s)), y_ref, norm, "int8 entry")
+    assert_close(host(q4k.q4k_gemm_h16(w, rows, cols, qh, dh, sh)), y_ref, norm, "h16 entry")
+    dots = O.block_dots(f["q"], rq)
+    assert np.array_equal(host(q4k.q4k_gemm_blockdots(w, rows, cols, q)), dots)
+    assert np.array_equal(host(q4k.q4k_gemm_blockdots_h16(w, rows, cols, qh)), dots)
+
+
+@pytest.mark.parametrize("tokens", [8, 48])
+def test_gemm_block_dots_at_the_extremes(tokens):
     # rows 0-7 hold q = 15 everywhere and tokens 0-3 are all +1 or all -1, so
     # those block dots reach the extreme +-15*127*32; the rest are mixed.
-    rows, cols, tokens = 16, 512, 8
+    # (8 tokens run the q8_1 GEMV, 48 the tensor-core kernel.)
+    rows, cols = 16, 512
     f = synth.q4k_fields(rows, cols, 90)
     f["q"][:8] = 15
     f["q"][8:, ::7] = 0

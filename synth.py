@@ -46,6 +46,22 @@ def draw_fields(rng: np.random.Generator, rows: int, cols: int) -> dict:
     return {"d": d, "dmin": dmin, "sc": sc, "m": m, "q": q}
 
 
+def draw_q6k_fields(rng: np.random.Generator, rows: int, cols: int) -> dict:
+    """Q6_K fields of one matrix: ``d = |N(0, 0.01)|`` (binary16 bits,
+    ``[rows][cols/256]``), ``sc`` uniform int8 -128..127 (``[rows][cols/16]``),
+    ``q`` uniform 0..63 (``[rows][cols]``); drawn in that order."""
+    if cols % QK_K:
+        raise ValueError(f"cols={cols} is not a multiple of {QK_K}")
+    d = np.abs(rng.normal(0.0, 0.01, (rows, cols // QK_K))).astype(np.float16).view(np.uint16)
+    sc = rng.integers(-128, 128, (rows, cols // 16), dtype=np.int16).astype(np.int8)
+    q = rng.integers(0, 64, (rows, cols), dtype=np.uint8)
+    return {"d": d, "sc": sc, "q": q}
+
+
+def q6k_fields(rows: int, cols: int, seed) -> dict:
+    return draw_q6k_fields(_rng(seed), rows, cols)
+
+
 def draw_activations(rng: np.random.Generator, n: int, cols: int) -> np.ndarray:
     return rng.standard_normal((n, cols), dtype=np.float32)
 

@@ -532,6 +532,35 @@ def run_ours(args, rank, world):
 
     q8_decode = {f"batch{b}": q8_layers(b) for b in (1, 4, 8)}
 
+    # ---------------- Q6_K decode GEMV (GPU layout): the Q6_K matrices of a
+    # Q4_K_M Qwen3-4B -- the output head and a down projection
+    def q6k_case(rows, cols, batch, seed, calls=12, reps=10):
+        f = synth.q6k_fields(rows, cols, seed)
+        w = q4k.q6k_pack(torch.from_numpy(f["d"].view(np.int16)).to(dev), torch.from_numpy(f["sc"]).to(dev),
+                         torch.from_numpy(f["q"]).to(dev))
+        del f
+        n_c = max(2, math.ceil(4 * l2 / w.numel()))
+        wc = [w] + [w.clone() for _ in range(n_c - 1)]
+        x = torch.from_numpy(synth.activations(batch, cols, [seed, 1])).to(dev)
+        y = torch.empty((batch, rows), device=dev)
+
+        def run():
+            for i in range(calls):
+                q4k.q6k_gemv(wc[i % n_c], rows, cols, x, y=y)
+        run()
+        torch.cuda.synchronize()
+        ms = time_graph(capture(run), reps) / calls
+        alg = rows * (cols // 256) * 210 + batch * (rows + cols) * 4
+        del wc, w
+        return {"rows": rows, "cols": cols, "batch": batch, "us": 1e3 * ms, "GB/s": alg / (ms * 1e-3) / 1e9,
+                "frac_of_measured_hbm": alg / (ms * 1e-3) / 1e9 / hbm_peak, "weight_copies": n_c}
+
+    q6k_decode = {"output_head_151936x2560_b1": q6k_case(151936, 2560, 1, 760),
+                  "down_2560x9728_b1": q6k_case(2560, 9728, 1, 761, calls=40),
+                  "down_2560x9728_b4": q6k_case(2560, 9728, 4, 762, calls=40),
+                  "v_1024x2560_b1": q6k_case(1024, 2560, 1, 763, calls=60)}
+    torch.cuda.empty_cache()
+
     # ---------------- single 2048x2048 GEMV, batch 1 (L2-resident: latency)
     f0, x0 = synth.single_gemv_2048(0)
     d0 = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev) for k, v in f0.items()}
@@ -720,6 +749,10 @@ def run_ours(args, rank, world):
                                           "GB/s": step_bytes * args.steps / (ms_chain * 1e-3) / 1e9},
             "token_36_layers_gemv_seq_with_waits": token_engine},
         "decode_q8_1_gemv_per_layer": q8_decode,
+        "decode_q6k_gemv": {**q6k_decode,
+                            "note": "q6k_gemv launches over Q6K_LAYOUT_GPU weights, rotating copies (inputs larger "
+                                    "than L2), median of graph replays; algorithmic bytes = 210 per 256 weights "
+                                    "+ x + y"},
         "decode_stack_36_layers_independent_jobs": {
             "note": "the 252 GEMVs of the stack with no dependencies between them (not a decode token)",
             **stack_indep},

@@ -363,6 +363,79 @@ int q4k_gemm_blockdots_h16(const void* w, int layout, int64_t rows, int64_t cols
                            void* stream);
 
 /*
+ * Q6_K weights (genie-ai-runtime §2: Q4_K_M models keep some matrices in
+ * Q6_K; §6 "The negatives I kept", Path G: a Q6_K block layout redesigned
+ * for vectorised loads is the open attack on Q6_K decode).  The pages print
+ * no Q6_K layout; the common GGUF Q6_K block is used: 256 weights with a
+ * binary16 scale d, sixteen int8 scales sc (one per 16 weights) and a 6-bit
+ * quant q per weight, w = d * sc * (q - 32).
+ *  - Q6K_LAYOUT_GGUF: 210-byte superblocks in GGUF byte order (ql[128] low
+ *    nibbles, qh[64] high bit pairs, scales[16], d), rows * cols/256 * 210
+ *    bytes.  210 is not a multiple of 16, so superblocks do not start on
+ *    16-byte boundaries and no tensor copy can fetch them: the GEMV does not
+ *    read this layout (Q4K_ERR_UNSUPPORTED); convert it with q6k_repack.
+ *  - Q6K_LAYOUT_GPU: per row, the row's superblocks as 208-byte blocks (the
+ *    16 scales, then per 64 weights 32 bytes of low nibbles and 16 bytes of
+ *    high bit pairs), then the row's d values, then zero padding to a
+ *    multiple of 16 bytes: rows * roundup16(cols/256 * 210) bytes, so the
+ *    padding is under 16 bytes a row.  The exact byte order is defined by
+ *    q6k_pack and read back by q6k_unpack.
+ */
+typedef enum q6k_layout {
+  Q6K_LAYOUT_GGUF = 0,
+  Q6K_LAYOUT_GPU = 1
+} q6k_layout;
+
+/* Bytes of a rows x cols Q6_K matrix in `layout`; 0 for an invalid request. */
+size_t q6k_packed_bytes(int64_t rows, int64_t cols, int layout);
+
+/*
+ * q6k_pack - pack Q6_K fields into `layout`:
+ *   d  : uint16 binary16 bits, [rows][cols/256]
+ *   sc : int8,                 [rows][cols/16]
+ *   q  : uint8 values 0..63,   [rows][cols]   (bits above 5 ignored)
+ *   w  : output, q6k_packed_bytes(rows, cols, layout) bytes
+ * Bit-exact.  Every pointer 16-byte aligned.
+ */
+int q6k_pack(const uint16_t* d, const int8_t* sc, const uint8_t* q, int64_t rows,
+             int64_t cols, int layout, void* w, void* stream);
+
+/*
+ * q6k_repack - convert packed Q6_K weights between layouts (a loader that
+ * reads GGUF blocks from a file calls it once per matrix with
+ * src_layout = Q6K_LAYOUT_GGUF, dst_layout = Q6K_LAYOUT_GPU).  src and dst
+ * must not overlap.  Bit-exact; a GGUF source needs only 2-byte alignment
+ * (its blocks are 210 bytes), every other pointer 16-byte alignment.
+ */
+int q6k_repack(const void* src, int src_layout, int64_t rows, int64_t cols,
+               void* dst, int dst_layout, void* stream);
+
+/*
+ * q6k_unpack - test export, the inverse of q6k_pack (fields as for
+ * q6k_pack; q comes back in its low 6 bits).  Alignment as for q6k_repack.
+ */
+int q6k_unpack(const void* w, int layout, int64_t rows, int64_t cols,
+               uint16_t* d, int8_t* sc, uint8_t* q, void* stream);
+
+/*
+ * q6k_gemv - decode GEMV over Q6_K weights in Q6K_LAYOUT_GPU (the same
+ * kernel as q4k_gemv, with the Q6_K superblock dot):
+ *   y[b][o] = sum_k w[o][k] * x[b][k]  (+ residual[b][o] if residual != NULL)
+ *   w        : Q6K_LAYOUT_GPU weights, rows x cols
+ *   x        : float [batch][cols], 1 <= batch <= 8
+ *   residual : float [batch][rows] or NULL
+ *   y        : float [batch][rows]; may alias residual, not x or w
+ * Accuracy: |y - exact| <= 1e-4 * (sum_k |w_k||x_k| + |residual|) per
+ * element, under the range condition at the top of this header (the quant
+ * enters the integer dot as the signed q - 32, so there is no second term).
+ * Arithmetic and determinism as q4k_gemv.  Q4K_ERR_UNSUPPORTED for a GGUF
+ * layout, batch > 8, or a shape whose staged activations do not fit.
+ */
+int q6k_gemv(const void* w, int layout, int64_t rows, int64_t cols,
+             const float* x, int64_t batch, const float* residual, float* y,
+             void* stream);
+
+/*
  * q4k_device_error - synchronise `stream` and read (then clear) the
  * library's device-side error word on the current device.  Returns Q4K_OK,
  * Q4K_ERR_DEVICE_TIMEOUT if a kernel abandoned a bounded wait since the last

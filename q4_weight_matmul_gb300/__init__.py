@@ -18,6 +18,8 @@ from .build import LIB_PATH, build
 
 BLOCK144 = 0
 LAYOUT_GPU = 1          # declared by the C ABI; every call refuses it (Q4K_ERR_UNSUPPORTED)
+Q6K_GGUF = 0            # Q6_K 210-byte GGUF superblocks
+Q6K_GPU = 1             # Q6_K GPU row layout (what q6k_gemv reads)
 Q4K_OK = 0
 QK_K = 256
 QK_SUB = 32
@@ -56,6 +58,11 @@ SIGNATURES = {
     "q4k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
     "q4k_gemm_h16": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
     "q4k_gemm_blockdots_h16": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
+    "q6k_packed_bytes": (ctypes.c_size_t, [_I64, _I64, _I]),
+    "q6k_pack": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P]),
+    "q6k_repack": (_I, [_P, _I, _I64, _I64, _P, _I, _P]),
+    "q6k_unpack": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _P]),
+    "q6k_gemv": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P, _P]),
     "q4k_device_error": (_I, [_P]),
     "q4k_selftest_wait_timeout": (_I, [_P]),
     "q4k_status_string": (ctypes.c_char_p, [_I]),
@@ -209,6 +216,56 @@ def q4k_gemv_q8(w, rows: int, cols: int, q8, d8, s, residual=None, y=None, layou
                              _ptr(d8, torch.float32, "d8"), _ptr(s, torch.int32, "sum"), batch,
                              _ptr(residual, torch.float32, "residual"), _ptr(y, torch.float32, "y"),
                              _stream(stream)), "q4k_gemv_q8")
+    return y
+
+
+def q6k_packed_bytes(rows: int, cols: int, layout: int = Q6K_GPU) -> int:
+    return int(lib().q6k_packed_bytes(rows, cols, layout))
+
+
+def q6k_pack(d, sc, q, out=None, layout: int = Q6K_GPU, stream=None):
+    """Pack Q6_K fields (binary16 d bits [rows][cols/256], int8 sc
+    [rows][cols/16], uint8 q [rows][cols]) into ``out`` (uint8,
+    ``q6k_packed_bytes`` long; allocated when None)."""
+    rows, cols = q.shape
+    if out is None:
+        out = torch.empty(q6k_packed_bytes(rows, cols, layout), dtype=torch.uint8, device=q.device)
+    _check(lib().q6k_pack(_ptr16(d, "d"), _ptr(sc, torch.int8, "sc"), _ptr(q, torch.uint8, "q"), rows, cols,
+                          layout, _ptr(out, torch.uint8, "out"), _stream(stream)), "q6k_pack")
+    return out
+
+
+def q6k_repack(src, rows: int, cols: int, src_layout: int = Q6K_GGUF, dst_layout: int = Q6K_GPU, out=None,
+               stream=None):
+    """Convert packed Q6_K weights between layouts (GGUF blocks to the GPU layout by default)."""
+    if out is None:
+        out = torch.empty(q6k_packed_bytes(rows, cols, dst_layout), dtype=torch.uint8, device=src.device)
+    _check(lib().q6k_repack(_ptr(src, torch.uint8, "src"), src_layout, rows, cols,
+                            _ptr(out, torch.uint8, "out"), dst_layout, _stream(stream)), "q6k_repack")
+    return out
+
+
+def q6k_unpack(w, rows: int, cols: int, layout: int = Q6K_GPU, stream=None):
+    """Test export: the fields of packed Q6_K weights, ``{"d"}`` (int16
+    binary16 bits), ``{"sc"}`` (int8) and ``{"q"}`` (uint8)."""
+    dev = w.device
+    out = {"d": torch.empty((rows, cols // QK_K), dtype=torch.int16, device=dev),
+           "sc": torch.empty((rows, cols // 16), dtype=torch.int8, device=dev),
+           "q": torch.empty((rows, cols), dtype=torch.uint8, device=dev)}
+    _check(lib().q6k_unpack(_ptr(w, torch.uint8, "w"), layout, rows, cols, _ptr16(out["d"], "d"),
+                            _ptr(out["sc"], torch.int8, "sc"), _ptr(out["q"], torch.uint8, "q"),
+                            _stream(stream)), "q6k_unpack")
+    return out
+
+
+def q6k_gemv(w, rows: int, cols: int, x, residual=None, y=None, layout: int = Q6K_GPU, stream=None):
+    """Decode GEMV over Q6_K weights (GPU layout): ``y[b] = W x[b] (+ residual[b])``."""
+    batch = x.shape[0]
+    if y is None:
+        y = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    _check(lib().q6k_gemv(_ptr(w, torch.uint8, "w"), layout, rows, cols, _ptr(x, torch.float32, "x"), batch,
+                          _ptr(residual, torch.float32, "residual"), _ptr(y, torch.float32, "y"),
+                          _stream(stream)), "q6k_gemv")
     return y
 
 

@@ -255,6 +255,86 @@ int q4k_gemv(const void* w, int layout, int64_t rows, int64_t cols, const float*
   return q4k_gemv_multi(1, &w, layout, &rows, cols, x, batch, res, ys, stream);
 }
 
+static bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+
+static int check_q6_layout(int layout) {
+  return (layout == Q6K_LAYOUT_GGUF || layout == Q6K_LAYOUT_GPU) ? Q4K_OK : Q4K_ERR_UNSUPPORTED;
+}
+
+size_t q6k_packed_bytes(int64_t rows, int64_t cols, int layout) {
+  if (check_rows(rows) || check_cols(cols) || check_q6_layout(layout)) return 0;
+  const int64_t nb = cols / kQK;
+  return layout == Q6K_LAYOUT_GGUF ? (size_t)rows * (size_t)nb * kQ6GgufBytes
+                                   : (size_t)rows * (size_t)q6k_gpu_row_bytes(nb);
+}
+
+// a packed buffer's alignment: 2 bytes for GGUF blocks, 16 for the GPU layout
+static bool q6_aligned(const void* w, int layout) {
+  return layout == Q6K_LAYOUT_GGUF ? aligned2(w) : aligned16(w);
+}
+
+int q6k_pack(const uint16_t* d, const int8_t* sc, const uint8_t* q, int64_t rows, int64_t cols, int layout,
+             void* w, void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_q6_layout(layout)) return e;
+  if (rows == 0) return Q4K_OK;
+  if (!d || !sc || !q || !w) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(d) || !aligned16(sc) || !aligned16(q) || !aligned16(w)) return Q4K_ERR_ALIGNMENT;
+  cudaError_t e = launch_q6k_convert(d, sc, q, nullptr, -1, rows, cols, nullptr, nullptr, nullptr,
+                                     static_cast<uint8_t*>(w), layout, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+int q6k_repack(const void* src, int src_layout, int64_t rows, int64_t cols, void* dst, int dst_layout,
+               void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_q6_layout(src_layout)) return e;
+  if (int e = check_q6_layout(dst_layout)) return e;
+  if (rows == 0) return Q4K_OK;
+  if (!src || !dst) return Q4K_ERR_INVALID_ARG;
+  if (!q6_aligned(src, src_layout) || !q6_aligned(dst, dst_layout)) return Q4K_ERR_ALIGNMENT;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  const size_t sn = q6k_packed_bytes(rows, cols, src_layout), dn = q6k_packed_bytes(rows, cols, dst_layout);
+  if (s0 < d0 + dn && d0 < s0 + sn) return Q4K_ERR_INVALID_ARG;   // overlap
+  cudaError_t e = launch_q6k_convert(nullptr, nullptr, nullptr, static_cast<const uint8_t*>(src), src_layout, rows,
+                                     cols, nullptr, nullptr, nullptr, static_cast<uint8_t*>(dst), dst_layout,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+int q6k_unpack(const void* w, int layout, int64_t rows, int64_t cols, uint16_t* d, int8_t* sc, uint8_t* q,
+               void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_q6_layout(layout)) return e;
+  if (rows == 0) return Q4K_OK;
+  if (!w || !d || !sc || !q) return Q4K_ERR_INVALID_ARG;
+  if (!q6_aligned(w, layout) || !aligned16(d) || !aligned16(sc) || !aligned16(q)) return Q4K_ERR_ALIGNMENT;
+  cudaError_t e = launch_q6k_convert(nullptr, nullptr, nullptr, static_cast<const uint8_t*>(w), layout, rows, cols,
+                                     d, sc, q, nullptr, -1, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+int q6k_gemv(const void* w, int layout, int64_t rows, int64_t cols, const float* x, int64_t batch,
+             const float* residual, float* y, void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_q6_layout(layout)) return e;
+  if (batch < 0) return Q4K_ERR_INVALID_ARG;
+  if (layout != Q6K_LAYOUT_GPU || batch > 8) return Q4K_ERR_UNSUPPORTED;
+  if (rows == 0 || batch == 0) return Q4K_OK;
+  if (!w || !x || !y) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)))
+    return Q4K_ERR_ALIGNMENT;
+  if (!gemv_q6k_supported(rows, cols, (int)batch)) return Q4K_ERR_UNSUPPORTED;
+  cudaError_t e = launch_gemv_q6k(static_cast<const uint8_t*>(w), rows, cols, x, (int)batch, residual, y,
+                                  static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return Q4K_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
 // Host-side checks of a q4k_gemv_seq request (no CUDA call).  Sets *work to
 // whether any job has work.
 static int check_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch, bool* work) {

@@ -514,5 +514,150 @@ __device__ __forceinline__ void superblock_dot_q8(const uint8_t* p, const uint8_
   for (int b = 0; b < B; ++b) acc[b] = fmaf(dm.x, scaled[b], -dm.y * mins[b]);
 }
 
+// ---------------------------------------------------------------------------
+// Q6_K superblocks in the GPU layout (q6k_pack.cu): 16 int8 scales, then four
+// 48-byte chunks of 64 weights -- 32 bytes of low nibbles (sub-block s = 0 in
+// the low nibble, s = 1 in the high, as in BLOCK144) and 16 bytes of high bit
+// pairs, pair f = 2s + h of byte i for position 16h + i of sub-block s, its
+// upper bit inverted.  The quant word for positions 16h+4k..+3 of sub-block s
+// is assembled as the signed bytes 4*(q - 32): the low nibble shifted to bits
+// 2-5 and the bit pair to bits 6-7, where the inverted pair reads as the
+// signed value hi - 2.  Each 16-weight scale group then takes the exact
+// integer 4*P per digit plane from four dp4a (|4P| <= 16*128*128).
+constexpr int kQ6Blk = 208;   // bytes of a GPU-layout Q6_K superblock
+
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int acc) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(acc));
+  return d;
+}
+
+// signed bytes 4*(q - 32) of sub-block s, half h, word k: l = low-nibble
+// word (h, k), hw = high-pair word k of the chunk
+__device__ __forceinline__ uint32_t q6_word(uint32_t l, uint32_t hw, int s, int h) {
+  const uint32_t lo = (s ? (l >> 2) : (l << 2)) & 0x3C3C3C3Cu;
+  const int f = 2 * s + h;
+  return ((hw << (6 - 2 * f)) & 0xC0C0C0C0u) | lo;
+}
+
+// sum over the 32 weights of sub-block j (0..7) of the Q6_K superblock at p
+// of sc_g * (q - 32) * x, in fp32 (the tier-3 path); activations as in
+// subblock_fp32
+template <bool kCoherent>
+__device__ __forceinline__ float subblock_fp32_q6(const uint8_t* p, int j, const float* xs, const float* xg) {
+  const uint8_t* ch = p + 16 + 48 * (j >> 1);
+  const int s = j & 1;
+  float v = 0.0f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float part = 0.0f;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int t = 16 * h + i;
+      const int lo = (ch[t] >> (4 * s)) & 15;
+      const int hi = (int)(((ch[32 + i] >> (2 * (2 * s + h))) & 3u) ^ 2u);
+      const float xl = xs ? xs[t] : (kCoherent ? __ldcg(xg + t) : __ldg(xg + t));
+      part = fmaf((float)(lo + 16 * hi - 32), xl, part);
+    }
+    v = fmaf((float)(int8_t)p[2 * j + h], part, v);
+  }
+  return v;
+}
+
+template <bool kCoherent>
+__device__ __noinline__ float tier3_fix_q6(const uint8_t* p, const XView X, int sb, int c0, int cpl, int b) {
+  const int nb = X.nb;
+  const uint16_t* tg = X.tag + ((size_t)b * nb + sb) * 8;
+  float add = 0.0f;
+  for (int j = 2 * c0; j < 2 * (c0 + cpl); ++j) {
+    const uint32_t t = tg[j];
+    if (!(t & 2u)) continue;
+    const float* xg = X.x + (size_t)b * nb * 256 + (size_t)sb * 256 + 32 * j;
+    const float* xs = (t >> 2) != kNoSlot ? X.pool3 + 32 * (size_t)(t >> 2) : nullptr;
+    add += subblock_fp32_q6<kCoherent>(p, j, xs, xg);
+  }
+  return add;
+}
+
+// superblock_dot for a Q6_K superblock (GPU layout, shared memory) with scale
+// d: acc[b] = d * sum_g sc_g s'_g V_g over the lane's chunks c0 .. c0+CPL-1,
+// V_g the group's P/256 in units of s' = 256 s (one rounding, as for Q4_K;
+// the factor 4 of the quant bytes is taken out by the combine's constants).
+// Tier-2 and tier-3 sub-blocks as in superblock_dot.
+template <int B, int CPL, bool kCoherent>
+__device__ __forceinline__ void superblock_dot_q6(const uint8_t* p, float d, const XView& X, int sb, int c0,
+                                                  float (&acc)[B]) {
+  const int nb = X.nb;
+  const uint4 scv = *reinterpret_cast<const uint4*>(p);   // int8 scales of groups 0..15
+  float scaled[B];
+#pragma unroll
+  for (int b = 0; b < B; ++b) scaled[b] = 0.0f;
+#pragma unroll
+  for (int cc = 0; cc < CPL; ++cc) {
+    const int c = c0 + cc;
+    const uint8_t* ch = p + 16 + 48 * c;
+    const uint4 hwv = *reinterpret_cast<const uint4*>(ch + 32);
+    const uint32_t scw = word_of(scv, c);   // groups 4c + 2s + h
+    const uint8_t* xc0 = X.planes + ((size_t)sb * 4 + c) * kRegion;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 lv = *reinterpret_cast<const uint4*>(ch + 16 * h);
+      uint32_t w0[4], w1[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w0[k] = q6_word(word_of(lv, k), word_of(hwv, k), 0, h);
+        w1[k] = q6_word(word_of(lv, k), word_of(hwv, k), 1, h);
+      }
+      const float sc0 = (float)(int8_t)((scw >> (8 * h)) & 0xFFu);
+      const float sc1 = (float)(int8_t)((scw >> (8 * (2 + h))) & 0xFFu);
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const uint4* xp = reinterpret_cast<const uint4*>(xc0 + (size_t)b * nb * 4 * kRegion) + h * 6;
+        int a0[3], a1[3];
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl) {
+          const uint4 xl = xp[2 * pl], xh = xp[2 * pl + 1];
+          a0[pl] = a1[pl] = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            a0[pl] = dp4a_ss(w0[k], word_of(xl, k), a0[pl]);
+            a1[pl] = dp4a_ss(w1[k], word_of(xh, k), a1[pl]);
+          }
+        }
+        const uint32_t tw = *reinterpret_cast<const uint32_t*>(X.tag + ((size_t)b * nb + sb) * 8 + 2 * c);
+        int p00 = 0, p01 = 0;
+        if (tw & 0x00010001u) {
+          if ((tw & 3u) == 1u) {
+            const uint4 xw = reinterpret_cast<const uint4*>(X.pool2 + 32 * (size_t)((tw >> 2) & 0x3FFFu))[h];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) p00 = dp4a_ss(w0[k], word_of(xw, k), p00);
+          }
+          if (((tw >> 16) & 3u) == 1u) {
+            const uint4 xw = reinterpret_cast<const uint4*>(X.pool2 + 32 * (size_t)(tw >> 18))[h];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) p01 = dp4a_ss(w1[k], word_of(xw, k), p01);
+          }
+        }
+        // (4P)/1024 = P/256 in units of s'
+        const float v0 = fmaf((float)(a0[2] * 256 + a0[1]), 64.0f, (float)(a0[0] * 256 + p00) * 0.0009765625f);
+        const float v1 = fmaf((float)(a1[2] * 256 + a1[1]), 64.0f, (float)(a1[0] * 256 + p01) * 0.0009765625f);
+        const float4 ss = *reinterpret_cast<const float4*>(X.ss + ((size_t)b * nb + sb) * 8 + 2 * c);
+        scaled[b] = fmaf(sc1 * ss.z, v1, fmaf(sc0 * ss.x, v0, scaled[b]));
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < B; ++b) acc[b] = d * scaled[b];
+#pragma unroll
+  for (int b = 0; b < B; ++b) {
+    const uint4 t8 = *reinterpret_cast<const uint4*>(X.tag + ((size_t)b * nb + sb) * 8);
+    uint32_t any;
+    if (CPL == 4) any = t8.x | t8.y | t8.z | t8.w;
+    else if (CPL == 2) any = c0 ? (t8.z | t8.w) : (t8.x | t8.y);
+    else any = word_of(t8, c0);
+    if (any & 0x00020002u) acc[b] = fmaf(d, tier3_fix_q6<kCoherent>(p, X, sb, c0, CPL, b), acc[b]);
+  }
+}
+
 }  // namespace gemv
 }  // namespace q4k

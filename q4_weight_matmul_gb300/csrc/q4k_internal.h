@@ -13,6 +13,8 @@ namespace q4k {
 constexpr int kQK = 256;         // weights per superblock
 constexpr int kSub = 32;         // weights per sub-block
 constexpr int kBlockBytes = 144; // bytes of one BLOCK144 superblock
+constexpr int kQ6GgufBytes = 210;  // bytes of one GGUF Q6_K superblock
+constexpr int kQ6GpuBytes = 208;   // bytes of one GPU-layout Q6_K superblock (d kept apart)
 
 // Device properties the launchers size their grids by (cached per device).
 struct DeviceInfo {
@@ -56,6 +58,17 @@ bool gemv_q8_supported(int64_t rows, int64_t cols, int batch);
 cudaError_t launch_gemv_q8_block144(const uint8_t* w, int64_t rows, int64_t cols, const void* q8, bool h16,
                                     const float* d8, const int32_t* sum, int batch, const float* residual,
                                     float* y, int32_t* p_out, cudaStream_t s);
+
+// Q6_K: bytes of one row in the GPU layout (nb superblocks), conversions
+// between fields (in_layout / out_layout -1), GGUF (0) and GPU (1) bytes,
+// and the decode GEMV over the GPU layout.
+int64_t q6k_gpu_row_bytes(int64_t nb);
+cudaError_t launch_q6k_convert(const uint16_t* d_in, const int8_t* sc_in, const uint8_t* q_in, const uint8_t* w_in,
+                               int in_layout, int64_t rows, int64_t cols, uint16_t* d_out, int8_t* sc_out,
+                               uint8_t* q_out, uint8_t* w_out, int out_layout, cudaStream_t s);
+bool gemv_q6k_supported(int64_t rows, int64_t cols, int batch);
+cudaError_t launch_gemv_q6k(const uint8_t* w, int64_t rows, int64_t cols, const float* x, int batch,
+                            const float* residual, float* y, cudaStream_t s);
 
 // Persistent GEMV over an ordered job list (q4k_gemv_seq).  Both return a
 // q4k_status; launch_gemv_seq stores the launch's CUDA error in *cuda_err.

@@ -6,6 +6,7 @@
     python -m q4_weight_matmul_gb300.profile_case q8 --tokens 512 --cols 9728
     python -m q4_weight_matmul_gb300.profile_case pack --rows 9728 --cols 2560
     python -m q4_weight_matmul_gb300.profile_case seq --layers 13 --batch 1 --reps 3
+    python -m q4_weight_matmul_gb300.profile_case q6k_gemv --rows 151936 --cols 2560 --batch 1 --reps 3
 
 ``seq`` runs --layers Qwen3-4B-shaped decode linear sets (q, k, v, o, gate,
 up, down; independent inputs) as one q4k_gemv_seq launch per rep, as the
@@ -58,7 +59,7 @@ def run_seq(a, dev, gen):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["gemv", "gemm", "gemm_h16", "q8", "pack", "seq"])
+    ap.add_argument("kernel", choices=["gemv", "gemm", "gemm_h16", "q8", "pack", "seq", "q6k_gemv"])
     ap.add_argument("--layers", type=int, default=13)
     ap.add_argument("--rows", type=int, default=9728)
     ap.add_argument("--cols", type=int, default=2560)
@@ -74,6 +75,21 @@ def main():
         run_seq(a, dev, gen)
         return
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
+    if a.kernel == "q6k_gemv":
+        d = (torch.rand((a.rows, a.cols // 256), generator=gen, device=dev) * 0.02).half().view(torch.int16)
+        sc = torch.randint(-128, 128, (a.rows, a.cols // 16), generator=gen, device=dev,
+                           dtype=torch.int16).to(torch.int8)
+        q = torch.randint(0, 64, (a.rows, a.cols), generator=gen, device=dev, dtype=torch.uint8)
+        w0 = q4k.q6k_pack(d, sc, q)
+        n = max(1, math.ceil(2 * l2 / w0.numel()))
+        ws = [w0] + [w0.clone() for _ in range(n - 1)]
+        x = torch.randn((a.batch, a.cols), device=dev, generator=gen)
+        y = torch.empty((a.batch, a.rows), device=dev)
+        for i in range(a.reps):
+            q4k.q6k_gemv(ws[i % n], a.rows, a.cols, x, y=y)
+        torch.cuda.synchronize()
+        print("profile case done:", a.kernel, a.rows, a.cols, a.batch, a.reps)
+        return
     f = rand_fields(a.rows, a.cols, dev, gen)
     w0 = q4k.q4k_pack(*f)
     n = max(1, math.ceil(2 * l2 / w0.numel())) if a.kernel in ("gemv", "gemm", "gemm_h16") else 1

@@ -27,12 +27,12 @@ def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
-    return sorted(set(re.findall(r"\b((?:q4k|q8)_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:q4k|q6k|q8)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for must in ("q4k_pack", "q8_quantize", "q4k_gemv", "q4k_gemm"):
+    for must in ("q4k_pack", "q8_quantize", "q4k_gemv", "q4k_gemm", "q6k_pack", "q6k_gemv"):
         assert must in names
 
 
@@ -59,6 +59,41 @@ def test_gpu_layout_is_declared_and_refused(lib):
     assert lib.q4k_unpack(fake, 1, 8, 256, fake, fake, fake, fake, fake, None) == 3
     assert lib.q4k_gemv(fake, 1, 8, 256, fake, 1, None, fake, None) == 3
     assert lib.q4k_gemm(fake, 1, 8, 256, fake, fake, fake, 16, fake, None) == 3
+
+
+def test_q6k_packed_bytes(lib):
+    # GGUF: 210 bytes a superblock; GPU layout: a row's 210*nb bytes padded to 16
+    assert lib.q6k_packed_bytes(151936, 2560, 0) == 151936 * 10 * 210
+    assert lib.q6k_packed_bytes(151936, 2560, 1) == 151936 * 2112
+    assert lib.q6k_packed_bytes(2560, 9728, 1) == 2560 * 7984
+    assert lib.q6k_packed_bytes(3, 2048, 1) == 3 * 1680                # 8 * 210, already a multiple of 16
+    assert lib.q6k_packed_bytes(0, 256, 1) == 0
+    assert lib.q6k_packed_bytes(4, 100, 1) == 0
+    assert lib.q6k_packed_bytes(4, 256, 2) == 0
+
+
+def test_q6k_validation_before_any_launch(lib):
+    fake, odd16, odd2 = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10002), ctypes.c_void_p(0x10001)
+    # the GEMV reads the GPU layout only
+    assert lib.q6k_gemv(fake, 0, 8, 256, fake, 1, None, fake, None) == 3
+    assert lib.q6k_gemv(fake, 1, 8, 256, fake, 9, None, fake, None) == 3
+    assert lib.q6k_gemv(fake, 1, 8, 256, fake, -1, None, fake, None) == 1
+    assert lib.q6k_gemv(fake, 1, 8, 300, fake, 1, None, fake, None) == 1
+    assert lib.q6k_gemv(None, 1, 8, 256, fake, 1, None, fake, None) == 1
+    assert lib.q6k_gemv(odd16, 1, 8, 256, fake, 1, None, fake, None) == 2
+    assert lib.q6k_gemv(None, 1, 0, 256, None, 1, None, None, None) == 0
+    assert lib.q6k_pack(fake, fake, fake, 2, 256, 5, fake, None) == 3
+    assert lib.q6k_pack(fake, fake, None, 2, 256, 1, fake, None) == 1
+    assert lib.q6k_pack(fake, fake, fake, 2, 256, 1, odd16, None) == 2
+    # a GGUF buffer needs 2-byte alignment only; the GPU layout 16
+    big = ctypes.c_void_p(0x100000)
+    assert lib.q6k_repack(odd2, 0, 2, 256, big, 1, None) == 2
+    assert lib.q6k_repack(fake, 0, 2, 256, odd16, 1, None) == 2
+    # overlapping source and destination
+    assert lib.q6k_repack(fake, 0, 2, 256, fake, 1, None) == 1
+    assert lib.q6k_unpack(fake, 3, 2, 256, fake, fake, fake, None) == 3
+    assert lib.q6k_unpack(fake, 1, 2, 256, fake, fake, odd16, None) == 2
+    assert lib.q6k_unpack(None, 1, 0, 256, None, None, None, None) == 0
 
 
 def test_q8_1_bytes(lib):

@@ -607,9 +607,10 @@ def run_ours(args, rank, world):
     def prefill_case(mats, xs_in, tokens, layers=1, rotate=True, form="h16"):
         """mats: [(name, fields, rows, cols, input)].  Times one step = q8_1 of
         every input + every GEMM, `layers` times over rotating weight copies.
-        form "h16": q8_quantize_h16 + q4k_gemm_h16; "int8": q8_quantize + q4k_gemm."""
-        quant = q4k.q8_quantize_h16 if form == "h16" else q4k.q8_quantize
-        gemm = q4k.q4k_gemm_h16 if form == "h16" else q4k.q4k_gemm
+        form "h16": q8_quantize_h16 + q4k_gemm_h16; "int8": q8_quantize + q4k_gemm;
+        "f16": x_split_f16 + q4k_gemm_f16 (fp16 activations, no q8_1 step)."""
+        quant = {"h16": q4k.q8_quantize_h16, "int8": q4k.q8_quantize, "f16": q4k.x_split_f16}[form]
+        gemm = {"h16": q4k.q4k_gemm_h16, "int8": q4k.q4k_gemm, "f16": q4k.q4k_gemm_f16}[form]
         w = {}
         for name, f, rows, cols, inp in mats:
             d = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev) for k, v in f.items()}
@@ -626,7 +627,10 @@ def run_ours(args, rank, world):
                 ws = wsets[L % n_c]
                 if not gemm_only:
                     for k, v in x.items():
-                        quant(v, *q8[k])
+                        if form == "f16":
+                            quant(v, out=q8[k])
+                        else:
+                            quant(v, *q8[k])
                 for name, _, rows, cols, inp in mats:
                     gemm(ws[name], rows, cols, *q8[inp], y=y[name])
 
@@ -649,6 +653,9 @@ def run_ours(args, rank, world):
     prefill512["workload"] = "512-token prefill: q8_1 X[512x2560] x gate 9728x2560, X_down[512x9728] x down 2560x9728"
     p512_int8 = prefill_case(mats512, pxs, 512, form="int8")
     prefill512["int8_entry_point"] = {k: p512_int8[k] for k in ("ms_per_step", "tok_s", "gemm_tops")}
+    p512_f16 = prefill_case(mats512, pxs, 512, form="f16")
+    prefill512["f16_activations"] = {k: p512_f16[k] for k in ("ms_per_step", "tok_s", "gemm_tops",
+                                                              "gemm_frac_of_bf16")}
     # short prompts (the pages' 18-33-token regime) on the same two matrices
     short = {}
     for T in (8, 16, 33, 64):
@@ -669,6 +676,8 @@ def run_ours(args, rank, world):
     mats8 = [(n, f8[n], rows, cols, inp) for n, rows, cols, inp in synth.QWEN3_8B_MLP]
     prefill8b = prefill_case(mats8, x8, 4096)
     prefill8b["workload"] = "4096-token prefill, Qwen3-8B MLP: gate/up 12288x4096, down 4096x12288"
+    p8_f16 = prefill_case(mats8, x8, 4096, form="f16")
+    prefill8b["f16_activations"] = {k: p8_f16[k] for k in ("ms_per_step", "tok_s", "gemm_tops", "gemm_frac_of_bf16")}
     del f8, x8
 
     # tensor-core rate probes on this GPU: the int8 rate of the warp-level

@@ -346,6 +346,40 @@ int q4k_gemm_h16(const void* w, int layout, int64_t rows, int64_t cols,
                  int64_t tokens, float* y, void* stream);
 
 /*
+ * x_split_f16 / q4k_gemm_f16 - the prefill GEMM in the fp16-operand form of
+ * genie-ai-runtime §3, "The tensor-core kernel (Path E)" (fp16 activations,
+ * fp32 accumulation), computing the product with the dequantised weights
+ * and fp32 activations directly (no q8_1 step):
+ *   y[t][o] = sum_k w[o][k] * x[t][k]
+ * x_split_f16 prepares the activations once per input (shared by every
+ * matrix that reads it): each token row t gets a power-of-two scale s_t
+ * that puts its largest |x| in [2^14, 2^15), and each X = s_t * x is held
+ * as hi = fp16(X) and lo = fp16(X - hi).
+ *   x         : float [tokens][cols]
+ *   hi, lo    : uint16 binary16 [tokens][cols]
+ *   bsum      : uint16 binary16 [tokens][cols/256][16]: per superblock the
+ *               eight 32-wide block sums of hi + lo, times 2^-6, as hi parts
+ *               then lo parts
+ *   inv_scale : float [tokens], 1/s_t
+ * x_split_f16_bytes gives the bytes of all four arrays together (0 for an
+ * invalid request).  q4k_gemm_f16 then runs the tensor-core GEMM over the
+ * split activations (any tokens >= 1; rows and cols as q4k_gemm):
+ *   y : float [tokens][rows]
+ * Accuracy: |y - exact| <= 1e-4 * (M + 2^-16 * max_k|x_k| * W1) per element,
+ * M the norm at the top of this header (fp32 x) and
+ * W1 = sum_k (|d*sc*q_k| + |dmin*m_k|): the hi/lo pair keeps each element
+ * to 2^-22 of itself, and elements below about 2^-24 of their row's largest
+ * are rounded in absolute terms (the second term).  Range as at the top of
+ * this header, for rows whose largest |x| lies in [2^-110, 2^110].
+ */
+size_t x_split_f16_bytes(int64_t tokens, int64_t cols);
+int x_split_f16(const float* x, int64_t tokens, int64_t cols, uint16_t* hi,
+                uint16_t* lo, uint16_t* bsum, float* inv_scale, void* stream);
+int q4k_gemm_f16(const void* w, int layout, int64_t rows, int64_t cols,
+                 const uint16_t* hi, const uint16_t* lo, const uint16_t* bsum,
+                 const float* inv_scale, int64_t tokens, float* y, void* stream);
+
+/*
  * q4k_gemm_blockdots - test export of the GEMM's per-block integer dots,
  * computed by the same tensor-core main loop as q4k_gemm:
  *   p[t][o][b] = sum_{i<32} q[o][32b+i] * q8[t][32b+i]

@@ -58,6 +58,9 @@ SIGNATURES = {
     "q4k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
     "q4k_gemm_h16": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
     "q4k_gemm_blockdots_h16": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
+    "x_split_f16_bytes": (ctypes.c_size_t, [_I64, _I64]),
+    "x_split_f16": (_I, [_P, _I64, _I64, _P, _P, _P, _P, _P]),
+    "q4k_gemm_f16": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _P, _I64, _P, _P]),
     "q6k_packed_bytes": (ctypes.c_size_t, [_I64, _I64, _I]),
     "q6k_pack": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P]),
     "q6k_repack": (_I, [_P, _I, _I64, _I64, _P, _I, _P]),
@@ -216,6 +219,35 @@ def q4k_gemv_q8(w, rows: int, cols: int, q8, d8, s, residual=None, y=None, layou
                              _ptr(d8, torch.float32, "d8"), _ptr(s, torch.int32, "sum"), batch,
                              _ptr(residual, torch.float32, "residual"), _ptr(y, torch.float32, "y"),
                              _stream(stream)), "q4k_gemv_q8")
+    return y
+
+
+def x_split_f16(x, out=None, stream=None):
+    """Split ``x`` [tokens][cols] float32 for ``q4k_gemm_f16``: returns
+    (hi, lo, bsum) as torch.float16 tensors and inv_scale float32 [tokens]."""
+    tokens, cols = x.shape
+    dev = x.device
+    if out is None:
+        out = (torch.empty((tokens, cols), dtype=torch.float16, device=dev),
+               torch.empty((tokens, cols), dtype=torch.float16, device=dev),
+               torch.empty((tokens, cols // QK_K, 16), dtype=torch.float16, device=dev),
+               torch.empty((tokens,), dtype=torch.float32, device=dev))
+    hi, lo, bs, inv = out
+    _check(lib().x_split_f16(_ptr(x, torch.float32, "x"), tokens, cols, _ptr(hi, torch.float16, "hi"),
+                             _ptr(lo, torch.float16, "lo"), _ptr(bs, torch.float16, "bsum"),
+                             _ptr(inv, torch.float32, "inv_scale"), _stream(stream)), "x_split_f16")
+    return out
+
+
+def q4k_gemm_f16(w, rows: int, cols: int, hi, lo, bsum, inv_scale, y=None, layout: int = BLOCK144, stream=None):
+    """fp16-activation prefill GEMM over ``x_split_f16`` output: ``y = x W^T``."""
+    tokens = hi.shape[0]
+    if y is None:
+        y = torch.empty((tokens, rows), dtype=torch.float32, device=hi.device)
+    _check(lib().q4k_gemm_f16(_ptr(w, torch.uint8, "w"), layout, rows, cols, _ptr(hi, torch.float16, "hi"),
+                              _ptr(lo, torch.float16, "lo"), _ptr(bsum, torch.float16, "bsum"),
+                              _ptr(inv_scale, torch.float32, "inv_scale"), tokens, _ptr(y, torch.float32, "y"),
+                              _stream(stream)), "q4k_gemm_f16")
     return y
 
 

@@ -455,6 +455,41 @@ int q4k_gemm_blockdots_h16(const void* w, int layout, int64_t rows, int64_t cols
   return gemm_h16_common(w, layout, rows, cols, q16, nullptr, nullptr, tokens, nullptr, p, stream);
 }
 
+size_t x_split_f16_bytes(int64_t tokens, int64_t cols) {
+  if (tokens < 0 || tokens > (int64_t(1) << 22) || check_cols(cols)) return 0;
+  return (size_t)tokens * ((size_t)cols * 4 + (size_t)(cols / kQK) * 32 + 4);
+}
+
+int x_split_f16(const float* x, int64_t tokens, int64_t cols, uint16_t* hi, uint16_t* lo, uint16_t* bsum,
+                float* inv_scale, void* stream) {
+  if (tokens < 0 || tokens > (int64_t(1) << 22)) return Q4K_ERR_INVALID_ARG;
+  if (int e = check_cols(cols)) return e;
+  if (tokens == 0) return Q4K_OK;
+  if (!x || !hi || !lo || !bsum || !inv_scale) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(hi) || !aligned16(lo) || !aligned16(bsum) || !aligned16(inv_scale))
+    return Q4K_ERR_ALIGNMENT;
+  cudaError_t e = launch_x_split_f16(x, tokens, cols, hi, lo, bsum, inv_scale, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+int q4k_gemm_f16(const void* w, int layout, int64_t rows, int64_t cols, const uint16_t* hi, const uint16_t* lo,
+                 const uint16_t* bsum, const float* inv_scale, int64_t tokens, float* y, void* stream) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_layout(layout)) return e;
+  if (tokens < 0 || tokens > (int64_t(1) << 22)) return Q4K_ERR_INVALID_ARG;
+  if (rows == 0 || tokens == 0) return Q4K_OK;
+  if (!w || !hi || !lo || !bsum || !inv_scale || !y) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(hi) || !aligned16(lo) || !aligned16(bsum) || !aligned16(inv_scale) ||
+      !aligned16(y))
+    return Q4K_ERR_ALIGNMENT;
+  int* err = device_error_word();
+  if (!err) return record_cuda(cudaGetLastError());
+  cudaError_t e = launch_gemm_f16(static_cast<const uint8_t*>(w), rows, cols, hi, lo, bsum, inv_scale, tokens, y,
+                                  err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
 size_t q4k_gemv_seq_workspace_bytes(const q4k_gemv_job* jobs, int n_jobs, int64_t batch) {
   bool work = false;
   if (check_seq(jobs, n_jobs, Q4K_LAYOUT_BLOCK144, batch, &work) != Q4K_OK || !work) return 0;

@@ -41,6 +41,7 @@
 // Every mbarrier wait is bounded (tc::kTimeoutCycles); a wait that gives up
 // sets the library's device error word, raises a CTA-wide abort flag and the
 // CTA unwinds, drains its MMAs and tensor copies and frees its TMEM.
+#include "mmq_cvt.cuh"
 #include "q4k_internal.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -105,44 +106,6 @@ __device__ __forceinline__ void split_bf16(float f, float& hi, float& lo) {
   lo = __bfloat162float(__float2bfloat16_rn(f - hi));
 }
 
-// One word of quant bytes (weights l..l+3 of the low sub-block in the low
-// nibbles, of the high sub-block in the high nibbles) -> sc*q fp16 pairs in
-// k order: (l, l+1), (l+2, l+3) of the low sub-block in lo0/lo1, of the high
-// sub-block in hi0/hi1.  Bytes go under the fp16 exponent of 1024 (low
-// nibble as 1024+q, high nibble as 1024+16q); one exact FMA removes the bias
-// and applies sc.
-__device__ __forceinline__ void cvt_q4x8(uint32_t w, uint32_t mlo, uint32_t alo, uint32_t mhi,
-                                         uint32_t ahi, uint32_t& lo0, uint32_t& lo1, uint32_t& hi0,
-                                         uint32_t& hi1) {
-  asm("{\n\t.reg .b32 t01, t23, z;\n\tmov.b32 z, 0;\n\t"
-      "prmt.b32 t01, %4, z, 0x4140;\n\tprmt.b32 t23, %4, z, 0x4342;\n\t"
-      "lop3.b32 %0, t01, 0x000F000F, 0x64006400, 0xEA;\n\t"
-      "lop3.b32 %1, t23, 0x000F000F, 0x64006400, 0xEA;\n\t"
-      "lop3.b32 %2, t01, 0x00F000F0, 0x64006400, 0xEA;\n\t"
-      "lop3.b32 %3, t23, 0x00F000F0, 0x64006400, 0xEA;\n\t"
-      "fma.rn.f16x2 %0, %0, %5, %6;\n\tfma.rn.f16x2 %1, %1, %5, %6;\n\t"
-      "fma.rn.f16x2 %2, %2, %7, %8;\n\tfma.rn.f16x2 %3, %3, %7, %8;\n\t}"
-      : "=r"(lo0), "=r"(lo1), "=r"(hi0), "=r"(hi1)
-      : "r"(w), "r"(mlo), "r"(alo), "r"(mhi), "r"(ahi));
-}
-
-// fp16x2 (v, v) of byte `bi` of w (an integer 0..255, exact): the byte
-// under the exponent of 1024, minus 1024
-__device__ __forceinline__ uint32_t byte_h2(uint32_t w, uint32_t bi) {
-  const uint32_t sel = bi | 0x40u | (bi << 8) | 0x4000u;   // bytes [bi, 0, bi, 0]
-  uint32_t r;
-  asm("{\n\t.reg .b32 t, z, k;\n\tmov.b32 z, 0;\n\tmov.b32 k, 0x64006400;\n\t"
-      "prmt.b32 t, %1, z, %2;\n\tor.b32 t, t, k;\n\tsub.rn.f16x2 %0, t, k;\n\t}"
-      : "=r"(r) : "r"(w), "r"(sel));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t mul_h2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 // acc += (a, b) * s2 as one fp32x2 FMA
 __device__ __forceinline__ void ffma2_acc(uint64_t& acc, uint32_t a, uint32_t b, uint64_t s2) {
   asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%1, %2};\n\tfma.rn.f32x2 %0, t, %3, %0;\n\t}"
@@ -160,14 +123,7 @@ __device__ __forceinline__ uint64_t pack2(float a, float b) {
   return (uint64_t)__float_as_uint(a) | ((uint64_t)__float_as_uint(b) << 32);
 }
 
-// packed 6-bit scales / mins of sub-blocks 0..3 and 4..7 of a header
-__device__ __forceinline__ void header_sc_m(const uint4& h, uint32_t& sc03, uint32_t& sc47, uint32_t& m03,
-                                            uint32_t& m47) {
-  sc03 = h.y & 0x3F3F3F3Fu;
-  m03 = h.z & 0x3F3F3F3Fu;
-  sc47 = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
-  m47 = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
-}
+using namespace cvt;
 
 struct GemmParams {
   CUtensorMap map_a;    // fp16 q8 {K, tokens}, box {64, 128}, 128-byte swizzle

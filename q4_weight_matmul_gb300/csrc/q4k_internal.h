@@ -101,6 +101,14 @@ cudaError_t launch_gemm_h16(const uint8_t* w, int64_t rows, int64_t cols, const 
                             const int32_t* sum, int64_t tokens, float* y, int32_t* p_out, int* err,
                             cudaStream_t s);
 
+// fp16-activation prefill GEMM: x split into per-token-scaled hi/lo binary16
+// parts and block sums (x_split_f16), then the tensor-core GEMM over them.
+cudaError_t launch_x_split_f16(const float* x, int64_t tokens, int64_t cols, uint16_t* hi, uint16_t* lo,
+                               uint16_t* bsum, float* inv_scale, cudaStream_t s);
+cudaError_t launch_gemm_f16(const uint8_t* w, int64_t rows, int64_t cols, const uint16_t* hi, const uint16_t* lo,
+                            const uint16_t* bsum, const float* inv_scale, int64_t tokens, float* y, int* err,
+                            cudaStream_t s);
+
 // One-thread kernel whose only (bounded) wait can never complete: after the
 // library's wait limit it records a timeout in `err` and returns.
 cudaError_t launch_wait_timeout_selftest(int* err, cudaStream_t s);

@@ -7,6 +7,7 @@
     python -m q4_weight_matmul_gb300.profile_case pack --rows 9728 --cols 2560
     python -m q4_weight_matmul_gb300.profile_case seq --layers 13 --batch 1 --reps 3
     python -m q4_weight_matmul_gb300.profile_case q6k_gemv --rows 151936 --cols 2560 --batch 1 --reps 3
+    python -m q4_weight_matmul_gb300.profile_case gemm_f16 --rows 9728 --cols 2560 --tokens 512
 
 ``seq`` runs --layers Qwen3-4B-shaped decode linear sets (q, k, v, o, gate,
 up, down; independent inputs) as one q4k_gemv_seq launch per rep, as the
@@ -59,7 +60,7 @@ def run_seq(a, dev, gen):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["gemv", "gemm", "gemm_h16", "q8", "pack", "seq", "q6k_gemv"])
+    ap.add_argument("kernel", choices=["gemv", "gemm", "gemm_h16", "gemm_f16", "q8", "pack", "seq", "q6k_gemv"])
     ap.add_argument("--layers", type=int, default=13)
     ap.add_argument("--rows", type=int, default=9728)
     ap.add_argument("--cols", type=int, default=2560)
@@ -92,7 +93,7 @@ def main():
         return
     f = rand_fields(a.rows, a.cols, dev, gen)
     w0 = q4k.q4k_pack(*f)
-    n = max(1, math.ceil(2 * l2 / w0.numel())) if a.kernel in ("gemv", "gemm", "gemm_h16") else 1
+    n = max(1, math.ceil(2 * l2 / w0.numel())) if a.kernel in ("gemv", "gemm", "gemm_h16", "gemm_f16") else 1
     ws = [w0] + [w0.clone() for _ in range(n - 1)]
     if a.kernel == "gemv":
         x = torch.randn((a.batch, a.cols), device=dev, generator=gen)
@@ -111,6 +112,12 @@ def main():
         y = torch.empty((a.tokens, a.rows), device=dev)
         for i in range(a.reps):
             q4k.q4k_gemm_h16(ws[i % n], a.rows, a.cols, q, d8, s, y=y)
+    elif a.kernel == "gemm_f16":
+        x = torch.randn((a.tokens, a.cols), device=dev, generator=gen)
+        sp = q4k.x_split_f16(x)
+        y = torch.empty((a.tokens, a.rows), device=dev)
+        for i in range(a.reps):
+            q4k.q4k_gemm_f16(ws[i % n], a.rows, a.cols, *sp, y=y)
     elif a.kernel == "q8":
         x = torch.randn((a.tokens, a.cols), device=dev, generator=gen)
         out = q4k.q8_quantize(x)

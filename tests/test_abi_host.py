@@ -27,7 +27,7 @@ def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
-    return sorted(set(re.findall(r"\b((?:q4k|q6k|q8)_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:q4k|q6k|q8|x_split)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -94,6 +94,21 @@ def test_q6k_validation_before_any_launch(lib):
     assert lib.q6k_unpack(fake, 3, 2, 256, fake, fake, fake, None) == 3
     assert lib.q6k_unpack(fake, 1, 2, 256, fake, fake, odd16, None) == 2
     assert lib.q6k_unpack(None, 1, 0, 256, None, None, None, None) == 0
+
+
+def test_f16_split_bytes_and_validation(lib):
+    # hi and lo: 2 bytes each per element; 16 binary16 block sums per superblock; 1/s per token
+    assert lib.x_split_f16_bytes(512, 2560) == 512 * (2560 * 4 + 10 * 32 + 4)
+    assert lib.x_split_f16_bytes(4, 100) == 0
+    fake, odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10008)
+    assert lib.x_split_f16(fake, 2, 300, fake, fake, fake, fake, None) == 1
+    assert lib.x_split_f16(fake, 2, 256, fake, fake, None, fake, None) == 1
+    assert lib.x_split_f16(fake, 2, 256, fake, odd, fake, fake, None) == 2
+    assert lib.x_split_f16(None, 0, 256, None, None, None, None, None) == 0
+    assert lib.q4k_gemm_f16(fake, 1, 8, 256, fake, fake, fake, fake, 4, fake, None) == 3   # GPU layout
+    assert lib.q4k_gemm_f16(fake, 0, 8, 256, fake, fake, None, fake, 4, fake, None) == 1
+    assert lib.q4k_gemm_f16(fake, 0, 8, 256, fake, fake, fake, fake, 4, odd, None) == 2
+    assert lib.q4k_gemm_f16(None, 0, 0, 256, None, None, None, None, 4, None, None) == 0
 
 
 def test_q8_1_bytes(lib):

@@ -28,7 +28,9 @@
 //
 // Tile: 128 tokens (TMEM lanes) x 128 weight rows (TMEM columns); K walks
 // 64 weights per stage, two A tiles (hi, lo) each one tensor copy into the
-// 128-byte-swizzled K-major layout.  Warp roles in one CTA of 14 warps:
+// 128-byte-swizzled K-major layout; six A tiles (three stages) are in flight
+// to cover the copies' latency.  The min-term operands of four consecutive
+// superblocks share one tile each (a 32-byte K slot per superblock).  Warp roles in one CTA of 14 warps:
 //   warp 0      lane 0 issues every tensor copy: A tiles, one raw 128-row x
 //               144-byte superblock tile per superblock, one block-sum tile
 //               per four superblocks
@@ -119,7 +121,7 @@ using namespace cvt;
 
 constexpr int kBM = 128;                 // tokens per tile
 constexpr int kBN = 128;                 // weight rows per tile
-constexpr int kATiles = 4;               // activation tiles in flight (hi, lo of two stages)
+constexpr int kATiles = 6;               // activation tiles in flight (hi, lo of three stages)
 constexpr int kBStages = 3;              // fp16 sc*q operand stages (converted)
 constexpr int kBRaw = 2;                 // raw superblock tiles in flight
 constexpr int kTileBytes = 128 * 128;    // 128 rows x 64 k x fp16
@@ -136,16 +138,16 @@ static_assert(kConvThreads == kBN, "one converter thread per weight row");
 struct __align__(1024) Smem {
   uint8_t a[kATiles][kTileBytes];          // fp16 hi / lo activations, 128B-swizzled (tensor copies)
   uint8_t b[kBStages][kTileBytes];         // fp16 sc*q, 128B-swizzled
-  uint8_t amin[2][kTileBytes];             // block sums of four superblocks (tensor copies)
-  uint8_t bmin[2][kTileBytes];             // [m | m] of one superblock (first 32 bytes of a row), by parity
+  uint8_t amin[kTileBytes];                // block sums of four superblocks (tensor copies), 32 bytes each
+  uint8_t bmin[kTileBytes];                // [m | m] of superblock sb in 32-byte slot sb % 4
   uint8_t braw[kBRaw][kBRawBytes];         // superblocks as copied
   float dsm[2][kBN];                       // d of each row, by superblock parity
   float dmsm[2][kBN];                      // 64 * dmin of each row
   uint64_t afull[kATiles], aempty[kATiles];
   uint64_t bfull[kBStages], bempty[kBStages];
   uint64_t rfull[kBRaw], rempty[kBRaw];
-  uint64_t amfull[2], amempty[2];
-  uint64_t bmfull[2], bmempty[2];
+  uint64_t amfull, amempty;
+  uint64_t bmfull[4], bmempty[4];
   uint64_t tfull[2], tempty[2];
   uint64_t dfull[2], dempty[2];
   uint64_t drain;
@@ -189,11 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
       tc::mbar_init(&sm.rfull[i], 1);
       tc::mbar_init(&sm.rempty[i], kConvThreads);
     }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sm.amfull[i], 1);
-      tc::mbar_init(&sm.amempty[i], 1);
+    tc::mbar_init(&sm.amfull, 1);
+    tc::mbar_init(&sm.amempty, 1);
+    for (int i = 0; i < 4; ++i) {
       tc::mbar_init(&sm.bmfull[i], kConvThreads);
       tc::mbar_init(&sm.bmempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&sm.tfull[i], 1);
       tc::mbar_init(&sm.tempty[i], kEpiWarps);
       tc::mbar_init(&sm.dfull[i], kConvThreads);
@@ -221,30 +225,49 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
     // --------------------------------------------------------- tensor copies
     if (lane == 0) {
       bool ok = true;
-      int na = 0, nr = 0, nm = 0;   // copies issued
+      int na = 0, nr = 0;           // copies issued
+      // The block-sum tile is single: group g is copied as soon as the MMAs
+      // of group g-1 are done with it.  Every wait below polls for that
+      // (without blocking), so the activation stream never stalls on it.
+      const int ngroups = (nb + 3) / 4;
+      int gnext = 0;
+      auto service = [&]() {
+        if (gnext < ngroups && tc::mbar_try_wait(&sm.amempty, (gnext & 1) ^ 1)) {
+          tc::mbar_arrive_expect_tx(&sm.amfull, kTileBytes);
+          tc::tma_load_2d(sm.amin, &P.map_bs, 64 * gnext, tok0, &sm.amfull);
+          ++gnext;
+        }
+      };
+      auto wait_serviced = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const long long t0 = clock64();
+        for (;;) {
+          if (tc::mbar_try_wait(bar, parity)) return true;
+          service();
+          if (*abort_flag || clock64() - t0 > tc::kTimeoutCycles) return false;
+        }
+      };
       for (int sb = 0; sb < nb && ok; ++sb) {
         {
           const int slot = sb % kBRaw;
-          if (!tc::mbar_wait(&sm.rempty[slot], ((sb / kBRaw) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          if (!wait_serviced(&sm.rempty[slot], ((sb / kBRaw) & 1) ^ 1)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(&sm.rfull[slot], kBRawBytes);
           tc::tma_load_3d(sm.braw[slot], &P.map_b, 0, row0, sb, &sm.rfull[slot]);
           ++nr;
         }
-        if ((sb & 3) == 0) {   // block sums of superblocks sb .. sb+3
-          const int g = sb >> 2, slot = g & 1;
-          if (!tc::mbar_wait(&sm.amempty[slot], ((g >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          tc::mbar_arrive_expect_tx(&sm.amfull[slot], kTileBytes);
-          tc::tma_load_2d(sm.amin[slot], &P.map_bs, 64 * g, tok0, &sm.amfull[slot]);
-          ++nm;
-        }
+        service();
         for (int i = 8 * sb; i < 8 * sb + 8; ++i) {   // tile i: stage i/2, hi (even) or lo (odd)
           const int slot = i % kATiles;
-          if (!tc::mbar_wait(&sm.aempty[slot], ((i / kATiles) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          if (!wait_serviced(&sm.aempty[slot], ((i / kATiles) & 1) ^ 1)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(&sm.afull[slot], kTileBytes);
           tc::tma_load_2d(sm.a[slot], (i & 1) ? &P.map_lo : &P.map_hi, 64 * (i >> 1), tok0, &sm.afull[slot]);
           ++na;
         }
       }
+      // the remaining block-sum groups
+      while (ok && gnext < ngroups) {
+        if (!wait_serviced(&sm.amempty, (gnext & 1) ^ 1)) ok = false;
+      }
+      const int nm = gnext;
       if (!ok) fail();
       // every copy issued lands before the CTA exits
       bool drained = true;
@@ -252,8 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
         drained &= tc::mbar_wait_sleep(&sm.afull[i % kATiles], (i / kATiles) & 1);
       for (int sb = nr - 1; sb >= 0 && sb >= nr - kBRaw; --sb)
         drained &= tc::mbar_wait_sleep(&sm.rfull[sb % kBRaw], (sb / kBRaw) & 1);
-      for (int g = nm - 1; g >= 0 && g >= nm - 2; --g)
-        drained &= tc::mbar_wait_sleep(&sm.amfull[g & 1], (g >> 1) & 1);
+      if (nm > 0) drained &= tc::mbar_wait_sleep(&sm.amfull, (nm - 1) & 1);
       if (!drained) fail();
     }
   } else if (warp == 1) {
@@ -285,18 +307,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
         if (!ok) break;
         // min term: this superblock's B_min and its group's block sums; the
         // epilogue has read the min accumulator of superblock sb - 1
-        const int g = sb >> 2;
-        if (!tc::mbar_wait(&sm.bmfull[buf], (sb >> 1) & 1, abort_flag) ||
-            !tc::mbar_wait(&sm.amfull[g & 1], (g >> 1) & 1, abort_flag) ||
+        const int g = sb >> 2, ms = sb & 3;
+        if (!tc::mbar_wait(&sm.bmfull[ms], g & 1, abort_flag) ||
+            !tc::mbar_wait(&sm.amfull, g & 1, abort_flag) ||
             (sb > 0 && !tc::mbar_wait(&sm.tempty[buf ^ 1], ((sb - 1) >> 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        tc::mma_f16_ss(tmem + kColMin, tc::desc_sw128(tc::smem_u32(sm.amin[g & 1]) + 32u * (uint32_t)(sb & 3)),
-                       tc::desc_sw128(tc::smem_u32(sm.bmin[buf])), idf, 0u);
-        tc::mma_commit(&sm.bmempty[buf]);
-        if ((sb & 3) == 3 || sb == nb - 1) tc::mma_commit(&sm.amempty[g & 1]);
+        tc::mma_f16_ss(tmem + kColMin, tc::desc_sw128(tc::smem_u32(sm.amin) + 32u * (uint32_t)ms),
+                       tc::desc_sw128(tc::smem_u32(sm.bmin) + 32u * (uint32_t)ms), idf, 0u);
+        tc::mma_commit(&sm.bmempty[ms]);
+        if (ms == 3 || sb == nb - 1) tc::mma_commit(&sm.amempty);
         tc::mma_commit(&sm.tfull[buf]);
       }
       if (!ok) fail();
@@ -315,13 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
       const uint4 hd = *reinterpret_cast<const uint4*>(raw_row);
       uint32_t sc03, sc47, m03, m47;
       header_sc_m(hd, sc03, sc47, m03, m47);
-      // B_min row ci: [m_0..m_7 | m_0..m_7] (k 0..15 of the min MMA)
-      if (!tc::mbar_wait(&sm.bmempty[par], ((sb >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+      // B_min row ci: [m_0..m_7 | m_0..m_7] (k 0..15 of the min MMA) in slot sb % 4
+      const int ms = sb & 3;
+      if (!tc::mbar_wait(&sm.bmempty[ms], ((sb >> 2) & 1) ^ 1, abort_flag)) { ok = false; break; }
       const uint4 mv = make_uint4(bytes_h2(m03, 0, 1), bytes_h2(m03, 2, 3), bytes_h2(m47, 0, 1), bytes_h2(m47, 2, 3));
-      *reinterpret_cast<uint4*>(sm.bmin[par] + tc::sw128_offset(ci, 0)) = mv;
-      *reinterpret_cast<uint4*>(sm.bmin[par] + tc::sw128_offset(ci, 1)) = mv;
+      *reinterpret_cast<uint4*>(sm.bmin + tc::sw128_offset(ci, 2 * ms)) = mv;
+      *reinterpret_cast<uint4*>(sm.bmin + tc::sw128_offset(ci, 2 * ms + 1)) = mv;
       tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&sm.bmfull[par]);
+      tc::mbar_arrive(&sm.bmfull[ms]);
       // d and 64*dmin of row ci, once the epilogue is done with superblock sb - 2
       if (!tc::mbar_wait(&sm.dempty[par], ((sb >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
       sm.dsm[par][ci] = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));

@@ -29,7 +29,8 @@
 // Tile: 128 tokens (TMEM lanes) x 128 weight rows (TMEM columns); K walks
 // 64 weights per stage, two A tiles (hi, lo) each one tensor copy into the
 // 128-byte-swizzled K-major layout; six A tiles (three stages) are in flight
-// to cover the copies' latency.  The min-term operands of four consecutive
+// to cover the copies' latency; one tcgen05.commit per stage releases the
+// stage's A and B tiles.  The min-term operands of four consecutive
 // superblocks share one tile each (a 32-byte K slot per superblock).  Warp roles in one CTA of 14 warps:
 //   warp 0      lane 0 issues every tensor copy: A tiles, one raw 128-row x
 //               144-byte superblock tile per superblock, one block-sum tile
@@ -134,6 +135,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColMin = 256;
 constexpr uint32_t kColTotal = 384;
 static_assert(kConvThreads == kBN, "one converter thread per weight row");
+static_assert(kATiles == 2 * kBStages, "an A stage (hi, lo) per B stage: one release per stage slot");
 
 struct __align__(1024) Smem {
   uint8_t a[kATiles][kTileBytes];          // fp16 hi / lo activations, 128B-swizzled (tensor copies)
@@ -143,8 +145,9 @@ struct __align__(1024) Smem {
   uint8_t braw[kBRaw][kBRawBytes];         // superblocks as copied
   float dsm[2][kBN];                       // d of each row, by superblock parity
   float dmsm[2][kBN];                      // 64 * dmin of each row
-  uint64_t afull[kATiles], aempty[kATiles];
-  uint64_t bfull[kBStages], bempty[kBStages];
+  uint64_t afull[kATiles];
+  uint64_t bfull[kBStages];
+  uint64_t sempty[kBStages];               // stage slot free: its two A tiles and its B tile
   uint64_t rfull[kBRaw], rempty[kBRaw];
   uint64_t amfull, amempty;
   uint64_t bmfull[4], bmempty[4];
@@ -179,13 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
   const int nb = P.nb, rows = P.rows, tokens = P.tokens;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kATiles; ++i) {
-      tc::mbar_init(&sm.afull[i], 1);
-      tc::mbar_init(&sm.aempty[i], 1);
-    }
+    for (int i = 0; i < kATiles; ++i) tc::mbar_init(&sm.afull[i], 1);
     for (int i = 0; i < kBStages; ++i) {
       tc::mbar_init(&sm.bfull[i], kConvThreads);
-      tc::mbar_init(&sm.bempty[i], 1);
+      tc::mbar_init(&sm.sempty[i], 1);   // one tcgen05.commit per stage releases its A and B tiles
     }
     for (int i = 0; i < kBRaw; ++i) {
       tc::mbar_init(&sm.rfull[i], 1);
@@ -256,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
         }
         service();
         for (int i = 8 * sb; i < 8 * sb + 8; ++i) {   // tile i: stage i/2, hi (even) or lo (odd)
-          const int slot = i % kATiles;
-          if (!wait_serviced(&sm.aempty[slot], ((i / kATiles) & 1) ^ 1)) { ok = false; break; }
+          const int slot = i % kATiles, j = i >> 1;
+          if ((i & 1) == 0 && !wait_serviced(&sm.sempty[j % kBStages], ((j / kBStages) & 1) ^ 1)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(&sm.afull[slot], kTileBytes);
           tc::tma_load_2d(sm.a[slot], (i & 1) ? &P.map_lo : &P.map_hi, 64 * (i >> 1), tok0, &sm.afull[slot]);
           ++na;
@@ -299,10 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
             for (int kk = 0; kk < 4; ++kk)
               tc::mma_f16_ss(tmem + 128u * buf, tc::desc_sw128(a_base + 32u * kk), tc::desc_sw128(b_base + 32u * kk),
                              idf, (c | part | kk) ? 1u : 0u);
-            tc::mma_commit(&sm.aempty[sa]);
           }
           if (!ok) break;
-          tc::mma_commit(&sm.bempty[sbs]);
+          // one release of the stage slot (A tiles and B tile): each
+          // tcgen05.commit costs the issuing thread, so one per stage
+          tc::mma_commit(&sm.sempty[sbs]);
         }
         if (!ok) break;
         // min term: this superblock's B_min and its group's block sums; the
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
         const uint4 q0 = *reinterpret_cast<const uint4*>(raw_row + 16 + 32 * c);
         const uint4 q1 = *reinterpret_cast<const uint4*>(raw_row + 32 + 32 * c);
         if (c == 3) tc::mbar_arrive(&sm.rempty[rslot]);
-        if (!tc::mbar_wait(&sm.bempty[slot], ((j / kBStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(&sm.sempty[slot], ((j / kBStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
         uint8_t* bt = sm.b[slot];
         // sub-blocks 2c (low nibbles, k 0..31 of the stage) and 2c+1 (high, k 32..63)
         const uint32_t scw = c < 2 ? sc03 : sc47;

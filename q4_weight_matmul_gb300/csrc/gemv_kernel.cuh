@@ -6,8 +6,8 @@
 // gate/up pair).
 //
 // Work split.  Rows are cut into blocks of RB rows (RB = 32, 16 or 8: the
-// tallest whose busiest SM holds at most 1/8 more rows than the fewest any
-// choice gives); one CTA per SM owns a run of
+// one whose busiest SM costs least, weighing each row by the instructions its
+// lanes spend per superblock); one CTA per SM owns a run of
 // row blocks (of one or several matrices) and all their superblocks.  A unit
 // of work is one row block x one superblock; the 15 consumer warps take units
 // round-robin, so K is split across warps.  Each unit leaves one partial sum
@@ -17,12 +17,11 @@
 // Streaming.  A producer warp fetches the weights with 3-D tensor copies:
 // one copy per stage of RB rows x (128/RB) superblocks (18 KB, out-of-range
 // rows and superblocks zero-filled) into a ring of stages.  The copies start
-// at launch, before the activations are read.  The CTA keeps its shared
-// memory under ~110 KB when it can; with 16 warps it may use 128 registers
-// per thread, so when launched as a programmatic dependent (opt-in, see
-// pdl_mode) the next GEMV's CTA starts on an SM once this one has left it;
-// griddepcontrol.wait orders every activation read after the previous kernel
-// has completed.
+// at launch, before the activations are read.  The ring is as deep as
+// shared memory allows (up to 6 stages); launched as a programmatic dependent
+// (opt-in, see pdl_mode) the CTA first keeps under ~110 KB so that the next
+// GEMV's CTA can start on its SM, and griddepcontrol.wait orders every
+// activation read after the previous kernel has completed.
 //
 // Lanes.  32/RB lanes share a row: with RB = 32 a lane owns a row's whole
 // superblock (256 weights), with RB = 16 half of it, with RB = 8 one 64-weight
@@ -338,23 +337,25 @@ struct Plan {
 Plan make_plan(int B, const int64_t* rows, int n_mats, int nb, const DeviceInfo& info, bool q8, int fmt) {
   const int stage_bytes = fmt == kFmtQ6K ? Fmt<kFmtQ6K>::kStage : Fmt<kFmtQ4K>::kStage;
   Plan p{};
-  // rows per block: the tallest block whose busiest SM holds at most 1/8 more
-  // rows than the best choice.  A lane that owns a whole superblock (32-row
-  // blocks) pays the per-unit costs (waits, scale decode, partial store) once
-  // per 256 weights, a quarter-superblock lane once per 64, so on a large
-  // matrix a few percent of row imbalance is cheaper than the shorter units.
-  int64_t busiest[3];
+  // rows per block: the choice whose busiest SM costs least, a row costing
+  // the instructions its lanes spend per superblock -- a lane that owns a whole
+  // superblock (32-row blocks) pays the per-unit costs (waits, scale decode,
+  // partial store, activation loads) once per 256 weights, a quarter-superblock
+  // lane once per 64 (measured: ~1.8x the instructions per weight with 8-row
+  // blocks, ~1.35x with 16-row blocks)
+  constexpr int64_t kCost[3] = {20, 27, 36};   // per row, 32-, 16-, 8-row blocks
   int64_t best = INT64_MAX;
+  p.lpr = 1;
   for (int i = 0; i < 3; ++i) {
     const int64_t rb = 32 >> i;
     int64_t n_rb = 0;
     for (int m = 0; m < n_mats; ++m) n_rb += (rows[m] + rb - 1) / rb;
-    busiest[i] = (n_rb + info.sm_count - 1) / info.sm_count * rb;
-    best = std::min(best, busiest[i]);
+    const int64_t cost = (n_rb + info.sm_count - 1) / info.sm_count * rb * kCost[i];
+    if (cost < best) {
+      best = cost;
+      p.lpr = 1 << i;
+    }
   }
-  p.lpr = 4;
-  for (int i = 2; i >= 0; --i)
-    if (8 * busiest[i] <= 9 * best) p.lpr = 1 << i;
   const int RB = 32 / p.lpr;
   int64_t n_rb = 0;
   for (int m = 0; m < n_mats; ++m) n_rb += (rows[m] + RB - 1) / RB;
@@ -362,10 +363,11 @@ Plan make_plan(int B, const int64_t* rows, int n_mats, int nb, const DeviceInfo&
   p.grid = (int)((n_rb + p.rb_per_cta - 1) / p.rb_per_cta);
   // partial sums of at most 8 KB per pass
   p.rb_pass = (int)std::max<int64_t>(1, std::min<int64_t>(p.rb_per_cta, 2048 / ((int64_t)B * nb * RB)));
-  // the deepest ring that keeps the CTA small enough to pair with the next
-  // kernel's; failing that, the deepest ring that fits at all
+  // the deepest ring that fits; launched as a programmatic dependent (opt-in),
+  // first the deepest that keeps the CTA small enough to share its SM with
+  // the next kernel's
   p.ring = 0;
-  const size_t caps[2] = {kPairSmem, (size_t)info.max_smem_optin};
+  const size_t caps[2] = {pdl_mode() != 0 ? kPairSmem : (size_t)info.max_smem_optin, (size_t)info.max_smem_optin};
   for (size_t cap : caps) {
     for (int ring = kMaxRing; ring >= 2 && p.ring == 0; --ring) {
       const size_t total = layout(B, nb, ring, B * p.rb_pass * nb * RB, q8, stage_bytes).total;

@@ -119,3 +119,25 @@ def test_gemm_f16_is_deterministic():
     b = q4k.q4k_gemm_f16(w, rows, cols, *sp)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("form", ["int8", "h16", "f16"])
+def test_gemm_writes_exactly_its_output(form):
+    """Canary: the GEMM writes every element of y and nothing around it
+    (ragged token and row tails: partial tiles at both edges)."""
+    rows, cols, tokens, pad = 300, 768, 130, 4096
+    f = synth.q4k_fields(rows, cols, 950)
+    w = pack_dev(f)
+    xd = torch.from_numpy(synth.activations(tokens, cols, 951)).cuda()
+    buf = torch.full((pad + tokens * rows + pad,), float("nan"), device="cuda")
+    y = buf[pad:pad + tokens * rows].view(tokens, rows)
+    if form == "f16":
+        q4k.q4k_gemm_f16(w, rows, cols, *q4k.x_split_f16(xd), y=y)
+    elif form == "h16":
+        q4k.q4k_gemm_h16(w, rows, cols, *q4k.q8_quantize_h16(xd), y=y)
+    else:
+        q4k.q4k_gemm(w, rows, cols, *q4k.q8_quantize(xd), y=y)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + tokens * rows:]).all(), "wrote outside y"
+    assert not torch.isnan(y).any(), "left part of y unwritten"
+    assert q4k.q4k_device_error() == 0

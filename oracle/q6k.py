@@ -25,6 +25,11 @@ common GGUF Q6_K block, restated in prose:
 Readings where the pages are silent (listed in the design notes): the
 dequantisation is evaluated in fp32 as ``(d * sc) * (q - 32)``; the GEMV
 accumulates in fp64; the tolerance is ``|y - y_ref| <= 1e-4 * sum |w||x|``.
+The MMQ form for q8_1 activations (the q8_1 block of 32 is the Q4_K path's,
+``oracle.q4k.quantize_q8_1``) takes one exact integer dot per 16-weight scale
+group, ``P = sum (q - 32) * q8``, and
+``y = sum_g d * sc_g * d8_(g/2) * P_g`` (no min term: the offset of 32 is in
+the integer dot).
 Pinned in ``tests/test_oracle_q6k.py``.
 """
 from __future__ import annotations
@@ -99,3 +104,32 @@ def gemv_q6k(fields: dict, x: np.ndarray, residual: np.ndarray | None = None):
         y = y + r
         norm = norm + np.abs(r)
     return y, norm
+
+
+def block_dots_q6k(q: np.ndarray, q8: np.ndarray) -> np.ndarray:
+    """``P[t][o][g] = sum_{i<16} (q[o][16g+i] - 32) * q8[t][16g+i]``, exact int64."""
+    q = np.asarray(q, np.int64) - 32
+    rows, cols = q.shape
+    n = np.asarray(q8).shape[0]
+    a = q.reshape(rows, cols // 16, 16)
+    b = np.asarray(q8).reshape(n, cols // 16, 16).astype(np.int64)
+    return np.einsum("ogi,tgi->tog", a, b)
+
+
+def mmq_q6k(fields: dict, q8: np.ndarray, d8: np.ndarray):
+    """Reference MMQ product over Q6_K weights and q8_1 activations:
+    ``y[t][o] = sum_g (d * sc_g)[o] * d8[t][g/2] * P[t][o][g]`` in float64
+    (``d * sc`` in fp32, as the dequantisation forms it).  Returns
+    ``(y_ref, norm)`` ``[tokens][rows]``, ``norm = sum_k |w||d8 q8|``."""
+    q = np.asarray(fields["q"], np.uint8)
+    rows, cols = q.shape
+    P = block_dots_q6k(q, q8).astype(np.float64)                       # [t][o][g]
+    d = f16_bits_to_f64(fields["d"]).astype(np.float32)                 # [o][nb]
+    dsc = (np.repeat(d, 16, axis=1) * np.asarray(fields["sc"], np.int8).astype(np.float32)).astype(np.float64)
+    d8g = np.repeat(np.asarray(d8, np.float32).astype(np.float64), 2, axis=1)   # [t][g]
+    y = np.einsum("tog,og,tg->to", P, dsc, d8g)
+    xh = (np.asarray(q8).reshape(q8.shape[0], cols // 32, 32).astype(np.float64)
+          * np.asarray(d8, np.float32).astype(np.float64)[:, :, None]).reshape(q8.shape[0], cols)
+    norm = np.abs(xh) @ np.abs(dequantize_q6k(fields).astype(np.float64)).T
+    return y, norm
+

@@ -131,3 +131,57 @@ def test_gemv_is_brute_force_on_a_tiny_integer_case():
             for k in range(256):
                 s += int(f["sc"][o, k // 16]) * (int(f["q"][o, k]) - 32) * int(x[b, k])
             assert y[b, o] == s
+
+
+def test_q6k_block_dots_by_brute_force_and_extremes():
+    rng = np.random.default_rng(16)
+    q = rng.integers(0, 64, (3, 256)).astype(np.uint8)
+    q8 = rng.integers(-127, 128, (2, 256)).astype(np.int8)
+    P = O6.block_dots_q6k(q, q8)
+    for t in range(2):
+        for o in range(3):
+            for g in range(16):
+                assert P[t, o, g] == sum((int(q[o, 16 * g + i]) - 32) * int(q8[t, 16 * g + i]) for i in range(16))
+    # extremes: q = 0 (-32) against +-127, and q = 63 (+31)
+    q[:] = 0
+    q8[:] = -127
+    assert np.all(O6.block_dots_q6k(q, q8) == 16 * 32 * 127)
+    q[:] = 63
+    q8[:] = 127
+    assert np.all(O6.block_dots_q6k(q, q8) == 16 * 31 * 127)
+
+
+def test_q6k_mmq_equals_the_fp_path_on_the_dequantised_activations():
+    """With x = d8 * q8 every MMQ term is the fp path's: the two agree to
+    rounding (and exactly when the scales are powers of two)."""
+    f = synth.q6k_fields(6, 768, 17)
+    x = synth.activations(3, 768, 18)
+    q8, d8, _ = O.quantize_q8_1(x)
+    y, norm = O6.mmq_q6k(f, q8, d8)
+    xh = O.dequantize_q8_1(q8, d8)                       # float64, exact
+    w = O6.dequantize_q6k(f).astype(np.float64)
+    y_fp, norm_fp = xh @ w.T, np.abs(xh) @ np.abs(w).T
+    assert np.array_equal(norm, norm_fp)
+    assert np.all(np.abs(y - y_fp) <= 1e-12 * norm)
+    f["d"][:] = 0x3C00                                   # d = 1: every factor exact
+    d8p = np.full_like(d8, 0.25)
+    y2, _ = O6.mmq_q6k(f, q8, d8p)
+    xh2 = O.dequantize_q8_1(q8, d8p)
+    assert np.array_equal(y2, xh2 @ O6.dequantize_q6k(f).astype(np.float64).T)
+
+
+def test_q6k_mmq_uses_the_scale_of_each_16_group_and_the_d8_of_its_32_block():
+    """One nonzero q8 element at a time: y equals d * sc_(k/16) * d8_(k/32) * (q_k - 32) * q8_k,
+    so a swapped scale group or block scale fails."""
+    f = synth.q6k_fields(2, 256, 19)
+    f["sc"] = np.arange(1, 17, dtype=np.int8)[None, :].repeat(2, axis=0)
+    d8 = (np.arange(1, 9, dtype=np.float32) * 0.5)[None, :]
+    d = O.f16_bits_to_f64(f["d"])
+    for k in (0, 15, 16, 31, 32, 200, 255):
+        q8 = np.zeros((1, 256), np.int8)
+        q8[0, k] = 3
+        y, _ = O6.mmq_q6k(f, q8, d8)
+        for o in range(2):
+            want = float(np.float32(np.float32(d[o, 0]) * np.float32(k // 16 + 1))) * float(d8[0, k // 32]) \
+                * (int(f["q"][o, k]) - 32) * 3
+            assert y[0, o] == want, (k, o)

@@ -534,7 +534,7 @@ def run_ours(args, rank, world):
 
     # ---------------- Q6_K decode GEMV (GPU layout): the Q6_K matrices of a
     # Q4_K_M Qwen3-4B -- the output head and a down projection
-    def q6k_case(rows, cols, batch, seed, calls=12, reps=10):
+    def q6k_case(rows, cols, batch, seed, calls=12, reps=10, q8=False):
         f = synth.q6k_fields(rows, cols, seed)
         w = q4k.q6k_pack(torch.from_numpy(f["d"].view(np.int16)).to(dev), torch.from_numpy(f["sc"]).to(dev),
                          torch.from_numpy(f["q"]).to(dev))
@@ -543,10 +543,14 @@ def run_ours(args, rank, world):
         wc = [w] + [w.clone() for _ in range(n_c - 1)]
         x = torch.from_numpy(synth.activations(batch, cols, [seed, 1])).to(dev)
         y = torch.empty((batch, rows), device=dev)
+        xq = q4k.q8_quantize(x) if q8 else None
 
         def run():
             for i in range(calls):
-                q4k.q6k_gemv(wc[i % n_c], rows, cols, x, y=y)
+                if q8:
+                    q4k.q6k_gemm(wc[i % n_c], rows, cols, *xq, y=y)
+                else:
+                    q4k.q6k_gemv(wc[i % n_c], rows, cols, x, y=y)
         run()
         torch.cuda.synchronize()
         ms = time_graph(capture(run), reps) / calls
@@ -558,7 +562,10 @@ def run_ours(args, rank, world):
     q6k_decode = {"output_head_151936x2560_b1": q6k_case(151936, 2560, 1, 760),
                   "down_2560x9728_b1": q6k_case(2560, 9728, 1, 761, calls=40),
                   "down_2560x9728_b4": q6k_case(2560, 9728, 4, 762, calls=40),
-                  "v_1024x2560_b1": q6k_case(1024, 2560, 1, 763, calls=60)}
+                  "v_1024x2560_b1": q6k_case(1024, 2560, 1, 763, calls=60),
+                  "down_2560x9728_q8_1_b1": q6k_case(2560, 9728, 1, 764, calls=40, q8=True),
+                  "down_2560x9728_q8_1_b8": q6k_case(2560, 9728, 8, 765, calls=40, q8=True),
+                  "down_2560x9728_q8_1_33_tokens": q6k_case(2560, 9728, 33, 766, calls=20, q8=True)}
     torch.cuda.empty_cache()
 
     # ---------------- single 2048x2048 GEMV, batch 1 (L2-resident: latency)
@@ -772,9 +779,10 @@ def run_ours(args, rank, world):
             "token_36_layers_gemv_seq_with_waits": token_engine},
         "decode_q8_1_gemv_per_layer": q8_decode,
         "decode_q6k_gemv": {**q6k_decode,
-                            "note": "q6k_gemv launches over Q6K_LAYOUT_GPU weights, rotating copies (inputs larger "
+                            "note": "q6k_gemv launches (fp32 activations) or q6k_gemm (q8_1 activations, one "
+                                    "launch per 8 tokens) over Q6K_LAYOUT_GPU weights, rotating copies (inputs larger "
                                     "than L2), median of graph replays; algorithmic bytes = 210 per 256 weights "
-                                    "+ x + y"},
+                                    "+ x + y (weights counted once per call)"},
         "decode_stack_36_layers_independent_jobs": {
             "note": "the 252 GEMVs of the stack with no dependencies between them (not a decode token)",
             **stack_indep},

@@ -470,6 +470,33 @@ int q6k_gemv(const void* w, int layout, int64_t rows, int64_t cols,
              void* stream);
 
 /*
+ * q6k_gemv_q8 / q6k_gemm - the MMQ product over Q6_K weights (Q6K_LAYOUT_GPU)
+ * and q8_1 activations (q8_quantize output; the block sums may be NULL, the
+ * Q6_K product has no min term):
+ *   y[t][o] = sum_g (d*sc_g)[o] * d8[t][g/2] * P[t][o][g]   (+ residual[t][o])
+ *   P[t][o][g] = sum_{i<16} (q[o][16g+i] - 32) * q8[t][16g+i]   (exact integers)
+ * q6k_gemv_q8 takes 1..8 token rows in one weight pass (batch decode, short
+ * prompts); q6k_gemm takes any token count as launches of up to 8 token rows
+ * each (the weights are read once per 8 tokens: the prefill of a few tokens
+ * and short prompts, not a tensor-core GEMM).  y: float [tokens][rows].
+ * Accuracy: |y - exact| <= 1e-4 * sum_k |w_k| |d8*q8_k| (+ |residual|).
+ * Deterministic.  All launches' shapes are checked before the first is
+ * enqueued.
+ */
+int q6k_gemv_q8(const void* w, int layout, int64_t rows, int64_t cols,
+                const int8_t* q8, const float* d8, const int32_t* sum,
+                int64_t batch, const float* residual, float* y, void* stream);
+int q6k_gemm(const void* w, int layout, int64_t rows, int64_t cols,
+             const int8_t* q8, const float* d8, const int32_t* sum,
+             int64_t tokens, float* y, void* stream);
+
+/* q6k_gemm_blockdots - test export of the exact group dots of q6k_gemm:
+ *   p : int32 [tokens][rows][cols/16], p[t][o][g] = P[t][o][g] above.
+ * Bit-exact. */
+int q6k_gemm_blockdots(const void* w, int layout, int64_t rows, int64_t cols,
+                       const int8_t* q8, int64_t tokens, int32_t* p, void* stream);
+
+/*
  * q4k_device_error - synchronise `stream` and read (then clear) the
  * library's device-side error word on the current device.  Returns Q4K_OK,
  * Q4K_ERR_DEVICE_TIMEOUT if a kernel abandoned a bounded wait since the last

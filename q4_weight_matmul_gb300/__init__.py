@@ -66,6 +66,9 @@ SIGNATURES = {
     "q6k_repack": (_I, [_P, _I, _I64, _I64, _P, _I, _P]),
     "q6k_unpack": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _P]),
     "q6k_gemv": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "q6k_gemv_q8": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P, _P]),
+    "q6k_gemm": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
+    "q6k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
     "q4k_device_error": (_I, [_P]),
     "q4k_selftest_wait_timeout": (_I, [_P]),
     "q4k_status_string": (ctypes.c_char_p, [_I]),
@@ -299,6 +302,38 @@ def q6k_gemv(w, rows: int, cols: int, x, residual=None, y=None, layout: int = Q6
                           _ptr(residual, torch.float32, "residual"), _ptr(y, torch.float32, "y"),
                           _stream(stream)), "q6k_gemv")
     return y
+
+
+def q6k_gemv_q8(w, rows: int, cols: int, q8, d8, s=None, residual=None, y=None, layout: int = Q6K_GPU, stream=None):
+    """MMQ GEMV over Q6_K weights and q8_1 activations (1..8 rows)."""
+    batch = q8.shape[0]
+    if y is None:
+        y = torch.empty((batch, rows), dtype=torch.float32, device=q8.device)
+    _check(lib().q6k_gemv_q8(_ptr(w, torch.uint8, "w"), layout, rows, cols, _ptr(q8, torch.int8, "q8"),
+                             _ptr(d8, torch.float32, "d8"), _ptr(s, torch.int32, "sum"), batch,
+                             _ptr(residual, torch.float32, "residual"), _ptr(y, torch.float32, "y"),
+                             _stream(stream)), "q6k_gemv_q8")
+    return y
+
+
+def q6k_gemm(w, rows: int, cols: int, q8, d8, s=None, y=None, layout: int = Q6K_GPU, stream=None):
+    """MMQ product over Q6_K weights for any number of q8_1 token rows."""
+    tokens = q8.shape[0]
+    if y is None:
+        y = torch.empty((tokens, rows), dtype=torch.float32, device=q8.device)
+    _check(lib().q6k_gemm(_ptr(w, torch.uint8, "w"), layout, rows, cols, _ptr(q8, torch.int8, "q8"),
+                          _ptr(d8, torch.float32, "d8"), _ptr(s, torch.int32, "sum"), tokens,
+                          _ptr(y, torch.float32, "y"), _stream(stream)), "q6k_gemm")
+    return y
+
+
+def q6k_gemm_blockdots(w, rows: int, cols: int, q8, layout: int = Q6K_GPU, stream=None):
+    """Test export: the exact 16-weight group dots [tokens][rows][cols/16] (int32)."""
+    tokens = q8.shape[0]
+    p = torch.empty((tokens, rows, cols // 16), dtype=torch.int32, device=q8.device)
+    _check(lib().q6k_gemm_blockdots(_ptr(w, torch.uint8, "w"), layout, rows, cols, _ptr(q8, torch.int8, "q8"),
+                                    tokens, _ptr(p, torch.int32, "p"), _stream(stream)), "q6k_gemm_blockdots")
+    return p
 
 
 def q4k_gemv_multi(ws, rows, cols: int, x, residuals=None, ys=None, layout: int = BLOCK144, stream=None):

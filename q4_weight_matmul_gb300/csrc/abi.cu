@@ -335,6 +335,66 @@ int q6k_gemv(const void* w, int layout, int64_t rows, int64_t cols, const float*
   return e == cudaSuccess ? Q4K_OK : record_cuda(e);
 }
 
+// shape and layout checks of the Q6_K q8_1 products (the GPU layout only)
+static int check_q6k_mmq(int layout, int64_t rows, int64_t cols) {
+  if (int e = check_rows(rows)) return e;
+  if (int e = check_cols(cols)) return e;
+  if (int e = check_q6_layout(layout)) return e;
+  return layout == Q6K_LAYOUT_GPU ? Q4K_OK : Q4K_ERR_UNSUPPORTED;
+}
+
+int q6k_gemv_q8(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8, const float* d8,
+                const int32_t* sum, int64_t batch, const float* residual, float* y, void* stream) {
+  if (int e = check_q6k_mmq(layout, rows, cols)) return e;
+  if (batch < 0 || batch > 8) return batch < 0 ? Q4K_ERR_INVALID_ARG : Q4K_ERR_UNSUPPORTED;
+  if (rows == 0 || batch == 0) return Q4K_OK;
+  if (!w || !q8 || !d8 || !y) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(q8) || !aligned16(d8) || (sum && !aligned16(sum)) || !aligned16(y) ||
+      (residual && !aligned16(residual)))
+    return Q4K_ERR_ALIGNMENT;
+  if (!gemv_q6k_q8_supported(rows, cols, (int)batch)) return Q4K_ERR_UNSUPPORTED;
+  cudaError_t e = launch_gemv_q6k_q8(static_cast<const uint8_t*>(w), rows, cols, q8, false, d8, nullptr, (int)batch,
+                                     residual, y, nullptr, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
+// q6k_gemm / q6k_gemm_blockdots: the MMQ product for any token count as
+// q8_1 GEMV launches of up to 8 tokens each
+static int q6k_gemm_common(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8, const float* d8,
+                           int64_t tokens, float* y, int32_t* p, void* stream) {
+  if (int e = check_q6k_mmq(layout, rows, cols)) return e;
+  if (tokens < 0 || tokens > (int64_t(1) << 22)) return Q4K_ERR_INVALID_ARG;
+  if (rows == 0 || tokens == 0) return Q4K_OK;
+  if (!w || !q8 || (!p && (!d8 || !y))) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(q8) || (d8 && !aligned16(d8)) || (y && !aligned16(y)) || (p && !aligned16(p)))
+    return Q4K_ERR_ALIGNMENT;
+  // every launch's shape is checked before the first is enqueued
+  const int64_t nsub = cols / kSub, ngrp = cols / 16;
+  if (!gemv_q6k_q8_supported(rows, cols, (int)std::min<int64_t>(tokens, 8)) ||
+      (tokens % 8 && !gemv_q6k_q8_supported(rows, cols, (int)(tokens % 8))))
+    return Q4K_ERR_UNSUPPORTED;
+  for (int64_t t0 = 0; t0 < tokens; t0 += 8) {
+    const int n = (int)std::min<int64_t>(8, tokens - t0);
+    cudaError_t e = launch_gemv_q6k_q8(static_cast<const uint8_t*>(w), rows, cols, q8 + t0 * cols, false,
+                                       d8 ? d8 + t0 * nsub : nullptr, nullptr, n, nullptr, y ? y + t0 * rows : nullptr,
+                                       p ? p + t0 * rows * ngrp : nullptr, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return record_cuda(e);
+  }
+  return Q4K_OK;
+}
+
+int q6k_gemm(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8, const float* d8,
+             const int32_t* sum, int64_t tokens, float* y, void* stream) {
+  (void)sum;   // the Q6_K product has no min term: the block sums are not read
+  return q6k_gemm_common(w, layout, rows, cols, q8, d8, tokens, y, nullptr, stream);
+}
+
+int q6k_gemm_blockdots(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8, int64_t tokens,
+                       int32_t* p, void* stream) {
+  if (!p && rows != 0 && tokens != 0) return Q4K_ERR_INVALID_ARG;
+  return q6k_gemm_common(w, layout, rows, cols, q8, nullptr, tokens, nullptr, p, stream);
+}
+
 // Host-side checks of a q4k_gemv_seq request (no CUDA call).  Sets *work to
 // whether any job has work.
 static int check_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch, bool* work) {

@@ -659,5 +659,60 @@ __device__ __forceinline__ void superblock_dot_q6(const uint8_t* p, float d, con
   }
 }
 
+// superblock_dot_q6 for q8_1 activations (the MMQ form): per 16-weight
+// group g the exact integer P_g = sum (q - 32) * q8 (dp4a on the 4*(q-32)
+// words, then /4), and acc[b] = d * sum_g sc_g * d8_(g/2) * P_g.  With
+// `pout` (test export) each P_g is stored at pout[b * pstride + g] (the
+// lane's groups only).
+template <int B, int CPL>
+__device__ __forceinline__ void superblock_dot_q6_q8(const uint8_t* p, float d, const uint8_t* xs,
+                                                     const float2* xss, int nb, int sb, int c0, float (&acc)[B],
+                                                     int32_t* pout, size_t pstride) {
+  const uint4 scv = *reinterpret_cast<const uint4*>(p);
+  float scaled[B];
+#pragma unroll
+  for (int b = 0; b < B; ++b) scaled[b] = 0.0f;
+#pragma unroll
+  for (int cc = 0; cc < CPL; ++cc) {
+    const int c = c0 + cc;
+    const uint8_t* ch = p + 16 + 48 * c;
+    const uint4 hwv = *reinterpret_cast<const uint4*>(ch + 32);
+    const uint32_t scw = word_of(scv, c);
+    const uint8_t* xc0 = xs + ((size_t)sb * 4 + c) * kRegionQ8;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 lv = *reinterpret_cast<const uint4*>(ch + 16 * h);
+      uint32_t w0[4], w1[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w0[k] = q6_word(word_of(lv, k), word_of(hwv, k), 0, h);
+        w1[k] = q6_word(word_of(lv, k), word_of(hwv, k), 1, h);
+      }
+      const float sc0 = (float)(int8_t)((scw >> (8 * h)) & 0xFFu);
+      const float sc1 = (float)(int8_t)((scw >> (8 * (2 + h))) & 0xFFu);
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const uint4* xp = reinterpret_cast<const uint4*>(xc0 + (size_t)b * nb * 4 * kRegionQ8) + h * 2;
+        const uint4 xl = xp[0], xh = xp[1];
+        int a0 = 0, a1 = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          a0 = dp4a_ss(w0[k], word_of(xl, k), a0);
+          a1 = dp4a_ss(w1[k], word_of(xh, k), a1);
+        }
+        const int p0 = a0 / 4, p1 = a1 / 4;   // exact: every product is a multiple of 4
+        const float4 ss = *reinterpret_cast<const float4*>(xss + ((size_t)b * nb + sb) * 8 + 2 * c);
+        scaled[b] = fmaf(sc1 * ss.z, (float)p1, fmaf(sc0 * ss.x, (float)p0, scaled[b]));
+        if (pout) {
+          pout[(size_t)b * pstride + 4 * c + h] = p0;
+          pout[(size_t)b * pstride + 4 * c + 2 + h] = p1;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < B; ++b) acc[b] = d * scaled[b];
+}
+
 }  // namespace gemv
 }  // namespace q4k

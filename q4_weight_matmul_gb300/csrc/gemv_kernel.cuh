@@ -140,7 +140,6 @@ __device__ __forceinline__ int mat_of(const GemvParams& P, int g) {
 template <int B, int LPR, int ACT, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
     const __grid_constant__ GemvParams P) {
-  static_assert(FMT == kFmtQ4K || ACT == kActF32, "Q6_K weights take fp32 activations");
   constexpr int RB = 32 / LPR;              // rows per block
   constexpr int kBlk = Fmt<FMT>::kBlk;
   constexpr int kStageBytes = Fmt<FMT>::kStage;
@@ -268,7 +267,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_block144_kernel(
           const __half* dv = reinterpret_cast<const __half*>(stages + (size_t)slot * kStageBytes +
                                                              Fmt<FMT>::kSuper * kBlk);
           const float dd = __half2float(dv[r_in * 8 + ((sj * SB) & 7) + z]);
-          gemv::superblock_dot_q6<B, CPL, false>(p, dd, xv, sb, c0, acc);
+          if constexpr (ACT == kActF32) {
+            gemv::superblock_dot_q6<B, CPL, false>(p, dd, xv, sb, c0, acc);
+          } else {
+            int32_t* pout = nullptr;
+            if (P.p_out) {
+              const int row = (rb0 + pb + rbl - P.rb_start[0]) * RB + r_in;
+              if (row < P.rows[0]) pout = P.p_out + ((size_t)row * nb + sb) * 16;
+            }
+            gemv::superblock_dot_q6_q8<B, CPL>(p, dd, xs, xss, nb, sb, c0, acc, pout, (size_t)P.rows[0] * nb * 16);
+          }
         } else if constexpr (ACT == kActF32) {
           gemv::superblock_dot<B, CPL, false>(p, xv, sb, c0, acc);
         } else {

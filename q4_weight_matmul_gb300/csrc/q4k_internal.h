@@ -69,6 +69,12 @@ cudaError_t launch_q6k_convert(const uint16_t* d_in, const int8_t* sc_in, const 
 bool gemv_q6k_supported(int64_t rows, int64_t cols, int batch);
 cudaError_t launch_gemv_q6k(const uint8_t* w, int64_t rows, int64_t cols, const float* x, int batch,
                             const float* residual, float* y, cudaStream_t s);
+// The same over q8_1 activations (MMQ form, 1..8 tokens); p_out (nullable)
+// receives the exact 16-weight group dots [batch][rows][cols/16].
+bool gemv_q6k_q8_supported(int64_t rows, int64_t cols, int batch);
+cudaError_t launch_gemv_q6k_q8(const uint8_t* w, int64_t rows, int64_t cols, const void* q8, bool h16,
+                               const float* d8, const int32_t* sum, int batch, const float* residual, float* y,
+                               int32_t* p_out, cudaStream_t s);
 
 // Persistent GEMV over an ordered job list (q4k_gemv_seq).  Both return a
 // q4k_status; launch_gemv_seq stores the launch's CUDA error in *cuda_err.

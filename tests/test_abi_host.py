@@ -94,6 +94,15 @@ def test_q6k_validation_before_any_launch(lib):
     assert lib.q6k_unpack(fake, 3, 2, 256, fake, fake, fake, None) == 3
     assert lib.q6k_unpack(fake, 1, 2, 256, fake, fake, odd16, None) == 2
     assert lib.q6k_unpack(None, 1, 0, 256, None, None, None, None) == 0
+    # the MMQ products read the GPU layout only; block sums may be NULL
+    assert lib.q6k_gemv_q8(fake, 0, 8, 256, fake, fake, None, 1, None, fake, None) == 3
+    assert lib.q6k_gemv_q8(fake, 1, 8, 256, fake, fake, None, 9, None, fake, None) == 3
+    assert lib.q6k_gemv_q8(fake, 1, 8, 256, None, fake, None, 1, None, fake, None) == 1
+    assert lib.q6k_gemv_q8(fake, 1, 8, 256, fake, fake, None, 1, None, odd16, None) == 2
+    assert lib.q6k_gemm(fake, 1, 8, 300, fake, fake, None, 4, fake, None) == 1
+    assert lib.q6k_gemm(fake, 1, 8, 256, fake, None, None, 4, fake, None) == 1
+    assert lib.q6k_gemm(None, 1, 0, 256, None, None, None, 4, None, None) == 0
+    assert lib.q6k_gemm_blockdots(fake, 1, 8, 256, fake, 4, None, None) == 1
 
 
 def test_f16_split_bytes_and_validation(lib):

@@ -201,3 +201,59 @@ def test_q6k_gemv_weak_staging_inputs(name, batch):
     torch.cuda.synchronize()
     check(y, f, x)
     assert q4k.q4k_device_error() == 0
+
+
+# --------------------------------------------------------- q8_1 activations
+def _q8(x):
+    q8, d8, s = O.quantize_q8_1(x)
+    return (q8, d8, s), tuple(torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in (q8, d8, s))
+
+
+@pytest.mark.parametrize("tokens", [1, 5, 8, 9, 17, 40])
+def test_q6k_gemm_group_dots_are_exact(tokens):
+    rows, cols = 77, 768
+    f = synth.q6k_fields(rows, cols, [760, tokens])
+    x = synth.activations(tokens, cols, [761, tokens])
+    (q8, _, _), (q8d, _, _) = _q8(x)
+    p = q4k.q6k_gemm_blockdots(pack_gpu(f), rows, cols, q8d)
+    torch.cuda.synchronize()
+    assert np.array_equal(p.cpu().numpy(), O6.block_dots_q6k(f["q"], q8))
+
+
+def test_q6k_group_dots_at_the_extremes():
+    """q = 0 and 63 (q - 32 = -32 and 31) against q8 = -127 and 127."""
+    rows, cols = 40, 512
+    f = synth.q6k_fields(rows, cols, 762)
+    f["q"][: rows // 2] = 0
+    f["q"][rows // 2:] = 63
+    q8 = np.where(np.arange(cols) % 3 == 0, 127, -127).astype(np.int8)[None, :].repeat(3, axis=0)
+    p = q4k.q6k_gemm_blockdots(pack_gpu(f), rows, cols, torch.from_numpy(q8).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(p.cpu().numpy(), O6.block_dots_q6k(f["q"], q8))
+
+
+@pytest.mark.parametrize("tokens,rows,cols", [(1, 1000, 2560), (4, 333, 2560), (8, 300, 9728),
+                                              (9, 130, 1024), (33, 2560, 9728), (40, 64, 256)])
+def test_q6k_gemm_parity(tokens, rows, cols):
+    f = synth.q6k_fields(rows, cols, [763, rows, tokens])
+    x = synth.activations(tokens, cols, [764, tokens])
+    (q8, d8, _), (q8d, d8d, sd) = _q8(x)
+    y = q4k.q6k_gemm(pack_gpu(f), rows, cols, q8d, d8d, sd)
+    torch.cuda.synchronize()
+    ok, worst = O.within_tolerance(y.cpu().numpy(), *O6.mmq_q6k(f, q8, d8), REL)
+    assert ok, f"{worst:.3g} x the allowed error"
+
+
+@pytest.mark.parametrize("batch", [1, 3, 8])
+def test_q6k_gemv_q8_with_residual_and_without_sums(batch):
+    rows, cols = 2560, 9728
+    f = synth.q6k_fields(rows, cols, [765, batch])
+    x = synth.activations(batch, cols, [766, batch])
+    r = synth.residual(batch, rows, [767, batch])
+    (q8, d8, _), (q8d, d8d, _) = _q8(x)
+    y = q4k.q6k_gemv_q8(pack_gpu(f), rows, cols, q8d, d8d, None, residual=torch.from_numpy(r).cuda())
+    torch.cuda.synchronize()
+    y_ref, norm = O6.mmq_q6k(f, q8, d8)
+    ok, worst = O.within_tolerance(y.cpu().numpy(), y_ref + r, norm + np.abs(r), REL)
+    assert ok, f"{worst:.3g} x the allowed error"
+    assert q4k.q4k_device_error() == 0

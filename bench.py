@@ -700,6 +700,40 @@ def run_ours(args, rank, world):
     prefill8b["f16_activations"] = {k: p8_f16[k] for k in ("ms_per_step", "tok_s", "gemm_tops", "gemm_frac_of_bf16")}
     del f8, x8
 
+    # Q6_K prefill: the down projection (Q6_K in Q4_K_M) at 512 tokens through
+    # the fp16-activation tensor-core GEMM, and through the q8_1 GEMV launches
+    def q6k_prefill(rows, cols, tokens, seed, reps=10):
+        f = synth.q6k_fields(rows, cols, seed)
+        w = q4k.q6k_pack(torch.from_numpy(f["d"].view(np.int16)).to(dev), torch.from_numpy(f["sc"]).to(dev),
+                         torch.from_numpy(f["q"]).to(dev))
+        del f
+        n_c = max(2, math.ceil(4 * l2 / w.numel()))
+        wc = [w] + [w.clone() for _ in range(n_c - 1)]
+        x = torch.from_numpy(synth.activations(tokens, cols, [seed, 1])).to(dev)
+        y = torch.empty((tokens, rows), device=dev)
+        sp = q4k.x_split_f16(x)
+        xq = q4k.q8_quantize(x)
+        out = {}
+        for form in ("f16", "q8_1"):
+            def run(calls=6):
+                for i in range(calls):
+                    if form == "f16":
+                        q4k.q6k_gemm_f16(wc[i % n_c], rows, cols, *sp, y=y)
+                    else:
+                        q4k.q6k_gemm(wc[i % n_c], rows, cols, *xq, y=y)
+            run()
+            torch.cuda.synchronize()
+            ms = time_graph(capture(run), reps) / 6
+            out[form] = {"ms": ms, "tops": 2.0 * tokens * rows * cols / (ms * 1e-3) / 1e12,
+                         "tok_s": tokens / (ms * 1e-3)}
+        del wc, w
+        return {"tokens": tokens, "rows": rows, "cols": cols, **out,
+                "note": "GEMM only (x_split_f16 / q8_quantize outside the timed graph); q8_1 form = one q6k_gemv_q8 "
+                        "launch per 8 tokens"}
+
+    prefill_q6k = q6k_prefill(2560, 9728, 512, 780)
+    torch.cuda.empty_cache()
+
     # tensor-core rate probes on this GPU: the int8 rate of the warp-level
     # MMA (mma.sync m16n8k32 s8) and the fp16 rate of tcgen05.mma kind::f16
     from q4_weight_matmul_gb300 import peaks as tc_peaks
@@ -806,6 +840,7 @@ def run_ours(args, rank, world):
         },
         "prefill_short_prompts": short,
         "prefill_2048_stack": prefill2048,
+        "prefill_q6k_down_512": prefill_q6k,
         "prefill_4096_qwen3_8b_mlp": prefill8b,
     }
     print(json.dumps(line), flush=True)

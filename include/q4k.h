@@ -490,6 +490,18 @@ int q6k_gemm(const void* w, int layout, int64_t rows, int64_t cols,
              const int8_t* q8, const float* d8, const int32_t* sum,
              int64_t tokens, float* y, void* stream);
 
+/*
+ * q6k_gemm_f16 - the fp16-activation tensor-core prefill GEMM (as
+ * q4k_gemm_f16) over Q6K_LAYOUT_GPU weights, on x_split_f16 output (bsum may
+ * be NULL: the Q6_K product has no min term):
+ *   y[t][o] = sum_k w[o][k] * x[t][k],   w = d * sc * (q - 32)
+ * Accuracy: |y - exact| <= 1e-4 * (sum_k |w_k||x_k| + 2^-16 * max_k|x_k| *
+ * sum_k |w_k|) per element (the split's bound, as for q4k_gemm_f16).
+ */
+int q6k_gemm_f16(const void* w, int layout, int64_t rows, int64_t cols,
+                 const uint16_t* hi, const uint16_t* lo, const uint16_t* bsum,
+                 const float* inv_scale, int64_t tokens, float* y, void* stream);
+
 /* q6k_gemm_blockdots - test export of the exact group dots of q6k_gemm:
  *   p : int32 [tokens][rows][cols/16], p[t][o][g] = P[t][o][g] above.
  * Bit-exact. */

@@ -69,6 +69,7 @@ SIGNATURES = {
     "q6k_gemv_q8": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P, _P]),
     "q6k_gemm": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
     "q6k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
+    "q6k_gemm_f16": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _P, _I64, _P, _P]),
     "q4k_device_error": (_I, [_P]),
     "q4k_selftest_wait_timeout": (_I, [_P]),
     "q4k_status_string": (ctypes.c_char_p, [_I]),
@@ -324,6 +325,18 @@ def q6k_gemm(w, rows: int, cols: int, q8, d8, s=None, y=None, layout: int = Q6K_
     _check(lib().q6k_gemm(_ptr(w, torch.uint8, "w"), layout, rows, cols, _ptr(q8, torch.int8, "q8"),
                           _ptr(d8, torch.float32, "d8"), _ptr(s, torch.int32, "sum"), tokens,
                           _ptr(y, torch.float32, "y"), _stream(stream)), "q6k_gemm")
+    return y
+
+
+def q6k_gemm_f16(w, rows: int, cols: int, hi, lo, bsum, inv_scale, y=None, layout: int = Q6K_GPU, stream=None):
+    """fp16-activation tensor-core GEMM over Q6_K weights, on ``x_split_f16`` output."""
+    tokens = hi.shape[0]
+    if y is None:
+        y = torch.empty((tokens, rows), dtype=torch.float32, device=hi.device)
+    bs = None if bsum is None else _ptr(bsum, torch.float16, "bsum")
+    _check(lib().q6k_gemm_f16(_ptr(w, torch.uint8, "w"), layout, rows, cols, _ptr(hi, torch.float16, "hi"),
+                              _ptr(lo, torch.float16, "lo"), bs, _ptr(inv_scale, torch.float32, "inv_scale"),
+                              tokens, _ptr(y, torch.float32, "y"), _stream(stream)), "q6k_gemm_f16")
     return y
 
 

@@ -389,6 +389,22 @@ int q6k_gemm(const void* w, int layout, int64_t rows, int64_t cols, const int8_t
   return q6k_gemm_common(w, layout, rows, cols, q8, d8, tokens, y, nullptr, stream);
 }
 
+int q6k_gemm_f16(const void* w, int layout, int64_t rows, int64_t cols, const uint16_t* hi, const uint16_t* lo,
+                 const uint16_t* bsum, const float* inv_scale, int64_t tokens, float* y, void* stream) {
+  (void)bsum;   // the Q6_K product has no min term: the block sums are not read
+  if (int e = check_q6k_mmq(layout, rows, cols)) return e;
+  if (tokens < 0 || tokens > (int64_t(1) << 22)) return Q4K_ERR_INVALID_ARG;
+  if (rows == 0 || tokens == 0) return Q4K_OK;
+  if (!w || !hi || !lo || !inv_scale || !y) return Q4K_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(hi) || !aligned16(lo) || !aligned16(inv_scale) || !aligned16(y))
+    return Q4K_ERR_ALIGNMENT;
+  int* err = device_error_word();
+  if (!err) return record_cuda(cudaGetLastError());
+  cudaError_t e = launch_gemm_q6k_f16(static_cast<const uint8_t*>(w), rows, cols, hi, lo, inv_scale, tokens, y, err,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? Q4K_OK : record_cuda(e);
+}
+
 int q6k_gemm_blockdots(const void* w, int layout, int64_t rows, int64_t cols, const int8_t* q8, int64_t tokens,
                        int32_t* p, void* stream) {
   if (!p && rows != 0 && tokens != 0) return Q4K_ERR_INVALID_ARG;

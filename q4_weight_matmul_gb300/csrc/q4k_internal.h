@@ -114,6 +114,9 @@ cudaError_t launch_x_split_f16(const float* x, int64_t tokens, int64_t cols, uin
 cudaError_t launch_gemm_f16(const uint8_t* w, int64_t rows, int64_t cols, const uint16_t* hi, const uint16_t* lo,
                             const uint16_t* bsum, const float* inv_scale, int64_t tokens, float* y, int* err,
                             cudaStream_t s);
+// The same form over GPU-layout Q6_K weights (no min term, no block sums).
+cudaError_t launch_gemm_q6k_f16(const uint8_t* w, int64_t rows, int64_t cols, const uint16_t* hi, const uint16_t* lo,
+                                const float* inv_scale, int64_t tokens, float* y, int* err, cudaStream_t s);
 
 // One-thread kernel whose only (bounded) wait can never complete: after the
 // library's wait limit it records a timeout in `err` and returns.

@@ -103,6 +103,10 @@ def test_q6k_validation_before_any_launch(lib):
     assert lib.q6k_gemm(fake, 1, 8, 256, fake, None, None, 4, fake, None) == 1
     assert lib.q6k_gemm(None, 1, 0, 256, None, None, None, 4, None, None) == 0
     assert lib.q6k_gemm_blockdots(fake, 1, 8, 256, fake, 4, None, None) == 1
+    assert lib.q6k_gemm_f16(fake, 0, 8, 256, fake, fake, None, fake, 4, fake, None) == 3
+    assert lib.q6k_gemm_f16(fake, 1, 8, 256, fake, None, None, fake, 4, fake, None) == 1
+    assert lib.q6k_gemm_f16(fake, 1, 8, 256, fake, fake, None, fake, 4, odd16, None) == 2
+    assert lib.q6k_gemm_f16(None, 1, 0, 256, None, None, None, None, 4, None, None) == 0
 
 
 def test_f16_split_bytes_and_validation(lib):

@@ -257,3 +257,69 @@ def test_q6k_gemv_q8_with_residual_and_without_sums(batch):
     ok, worst = O.within_tolerance(y.cpu().numpy(), y_ref + r, norm + np.abs(r), REL)
     assert ok, f"{worst:.3g} x the allowed error"
     assert q4k.q4k_device_error() == 0
+
+
+
+# ------------------------------------------------ fp16-activation tensor-core GEMM
+def _f16_norm(f, x):
+    w = np.abs(O6.dequantize_q6k(f).astype(np.float64))
+    x64 = np.abs(np.asarray(x, np.float64))
+    return x64 @ w.T + 2.0 ** -16 * x64.max(axis=1, keepdims=True) * w.sum(axis=1)[None, :]
+
+
+@pytest.mark.parametrize("tokens,rows,cols", [
+    (1, 9, 256), (5, 128, 768), (128, 128, 2560), (130, 300, 2560), (200, 77, 1024),
+    (300, 260, 9728), (64, 1000, 512), (129, 129, 2304)])
+def test_q6k_gemm_f16_parity(tokens, rows, cols):
+    f = synth.q6k_fields(rows, cols, [770, rows, cols])
+    x = synth.activations(tokens, cols, [771, tokens])
+    y = q4k.q6k_gemm_f16(pack_gpu(f), rows, cols, *q4k.x_split_f16(torch.from_numpy(x).cuda()))
+    torch.cuda.synchronize()
+    y_ref, _ = O6.gemv_q6k(f, x)
+    ok, worst = O.within_tolerance(y.cpu().numpy(), y_ref, _f16_norm(f, x), REL)
+    assert ok, f"{worst:.3g} x the allowed error"
+
+
+def test_q6k_gemm_f16_extreme_weights():
+    """sc = -128 / 127 with q = 0 / 63: |sc (q - 32)| above 2048, where the
+    weight operand needs its low part."""
+    rows, cols, tokens = 64, 1024, 40
+    f = synth.q6k_fields(rows, cols, 772)
+    f["sc"][: rows // 2] = -128
+    f["sc"][rows // 2:] = 127
+    f["q"][:, ::2] = 0
+    f["q"][:, 1::2] = 63
+    x = synth.activations(tokens, cols, 773)
+    y = q4k.q6k_gemm_f16(pack_gpu(f), rows, cols, *q4k.x_split_f16(torch.from_numpy(x).cuda()))
+    torch.cuda.synchronize()
+    y_ref, _ = O6.gemv_q6k(f, x)
+    ok, worst = O.within_tolerance(y.cpu().numpy(), y_ref, _f16_norm(f, x), REL)
+    assert ok, f"{worst:.3g} x the allowed error"
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_q6k_gemm_f16_weak_staging_inputs(name):
+    f, x = CASES[name](3)
+    rows, cols = f["q"].shape
+    x = np.ascontiguousarray(np.tile(x, (45, 1)))     # 135 tokens: two token tiles
+    y = q4k.q6k_gemm_f16(pack_gpu(f), rows, cols, *q4k.x_split_f16(torch.from_numpy(x).cuda()))
+    torch.cuda.synchronize()
+    y_ref, _ = O6.gemv_q6k(f, x)
+    ok, worst = O.within_tolerance(y.cpu().numpy(), y_ref, _f16_norm(f, x), REL)
+    assert ok, f"{name}: {worst:.3g} x the allowed error"
+    assert q4k.q4k_device_error() == 0
+
+
+def test_q6k_gemm_f16_canary_and_determinism():
+    rows, cols, tokens, pad = 300, 768, 130, 4096
+    f = synth.q6k_fields(rows, cols, 774)
+    w = pack_gpu(f)
+    sp = q4k.x_split_f16(torch.from_numpy(synth.activations(tokens, cols, 775)).cuda())
+    buf = torch.full((pad + tokens * rows + pad,), float("nan"), device="cuda")
+    y = buf[pad:pad + tokens * rows].view(tokens, rows)
+    q4k.q6k_gemm_f16(w, rows, cols, *sp, y=y)
+    y2 = q4k.q6k_gemm_f16(w, rows, cols, *sp)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + tokens * rows:]).all()
+    assert not torch.isnan(y).any()
+    assert torch.equal(y, y2)

@@ -23,7 +23,8 @@
  *  - Device pointers must be 16-byte aligned (Q4K_ERR_ALIGNMENT otherwise).
  *  - Sizes of zero (rows, tokens, batch) are valid and enqueue nothing.
  *  - A call whose work takes more than one kernel launch (a q4k_gemv_seq
- *    list of more than 96 jobs) validates and plans all of it first; only a
+ *    list of more than 96 jobs, or 48 Q6_K jobs) validates and plans all of
+ *    it first; only a
  *    CUDA launch failure of a later launch can leave the earlier ones
  *    enqueued (the status is then Q4K_ERR_CUDA).
  *
@@ -220,7 +221,9 @@ typedef struct q4k_gemv_job {
   float* y;                /* float [batch][rows]; may alias residual           */
   int32_t wait;            /* non-zero: x and residual are read only after every
                               earlier job of the list has stored its y          */
-  int32_t reserved;        /* ignored; set to 0                                 */
+  int32_t format;          /* 0: Q4_K weights in the call's `layout`;
+                              1: Q6_K weights in Q6K_LAYOUT_GPU (the Q6_K
+                              superblock dot of q6k_gemv and its accuracy)     */
 } q4k_gemv_job;
 
 #define Q4K_GEMV_SEQ_MAX_JOBS 256
@@ -235,7 +238,7 @@ size_t q4k_gemv_seq_workspace_bytes(const q4k_gemv_job* jobs, int n_jobs, int64_
 
 /*
  * q4k_gemv_seq - an ordered list of decode GEMVs in ONE persistent launch
- * per 96 jobs (genie-ai-runtime §4, Path C: the GEMVs are the hot decode
+ * per 96 jobs, 48 of them Q6_K at most (genie-ai-runtime §4, Path C: the GEMVs are the hot decode
  * kernels, and every decode step streams the whole model's weights; §2:
  * decode is bound by memory bandwidth).  One CTA per SM streams the weights
  * of job after job without a launch boundary, each SM the same share of the
@@ -257,7 +260,9 @@ size_t q4k_gemv_seq_workspace_bytes(const q4k_gemv_job* jobs, int n_jobs, int64_
  *               share a workspace must not overlap on the GPU.
  * The launch is cooperative (every CTA resident at once, one per SM); it
  * fails with Q4K_ERR_CUDA when the GPU cannot hold them all.
- * Accuracy and arithmetic as q4k_gemv.
+ * Jobs may mix Q4_K and Q6_K weights (q4k_gemv_job.format): a Q4_K_M
+ * layer, whose down and v projections are Q6_K in half the layers, runs as
+ * one list.  Accuracy and arithmetic as q4k_gemv (Q6_K jobs: as q6k_gemv).
  * Deterministic: for one job list on one device, the same inputs give the
  * same bits on every run.
  * Errors: Q4K_ERR_INVALID_ARG (null pointer, bad size, workspace too small),
@@ -274,7 +279,8 @@ int q4k_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch
  * engine pre-allocates its pools and does no allocation or set-up on the
  * hot path, genie-ai-runtime §4 "Memory-first").
  *   plan_bytes = q4k_gemv_seq_plan_bytes(n_jobs): host bytes of a plan
- *     (about 32 KB per 96 jobs); 0 if n_jobs is out of range.
+ *     (room for one launch of about 28 KB per 48 jobs, the most Q6_K jobs
+ *     one launch takes); 0 if n_jobs is out of range.
  *   q4k_gemv_seq_plan validates the list exactly as q4k_gemv_seq does and
  *     writes the plan (tensor maps of every weight matrix, the work split,
  *     every device pointer of the jobs and the workspace) into `plan`:

@@ -34,7 +34,7 @@ GEMV_SEQ_MAX_JOBS = 256
 class GemvJob(ctypes.Structure):
     """``q4k_gemv_job`` of the C ABI (one GEMV of a ``q4k_gemv_seq`` list)."""
     _fields_ = [("w", _P), ("rows", _I64), ("cols", _I64), ("x", _P), ("residual", _P), ("y", _P),
-                ("wait", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("wait", ctypes.c_int32), ("format", ctypes.c_int32)]
 
 
 # Every symbol the header declares, with its ctypes signature.
@@ -378,6 +378,7 @@ def _job_array(jobs):
         arr[i].residual = _ptr(j.get("residual"), torch.float32, "residual")
         arr[i].y = _ptr(j["y"], torch.float32, "y")
         arr[i].wait = 1 if j.get("wait") else 0
+        arr[i].format = int(j.get("format", 0))      # 0 Q4_K, 1 Q6_K (GPU layout)
         dev = j["x"].device if dev is None else dev
     return arr, n, dev
 

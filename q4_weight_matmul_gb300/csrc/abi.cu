@@ -424,6 +424,7 @@ static int check_seq(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t b
     const q4k_gemv_job& j = jobs[i];
     if (int e = check_rows(j.rows)) return e;
     if (int e = check_cols(j.cols)) return e;
+    if (j.format != 0 && j.format != 1) return Q4K_ERR_INVALID_ARG;
     if (j.rows == 0) continue;
     if (!j.w || !j.x || !j.y) return Q4K_ERR_INVALID_ARG;
     if (!aligned16(j.w) || !aligned16(j.x) || !aligned16(j.y) || (j.residual && !aligned16(j.residual)))

@@ -1,5 +1,5 @@
 // q4k_gemv_seq: an ordered list of decode GEMV jobs y = W x (+ residual) over
-// BLOCK144 Q4_K weights in one persistent launch (genie-ai-runtime §4,
+// BLOCK144 Q4_K (or GPU-layout Q6_K) weights in one persistent launch (genie-ai-runtime §4,
 // Path C: the GEMVs are the hot decode kernels and every decode step streams
 // the whole model; §2: decode is bound by memory bandwidth).
 //
@@ -35,8 +35,13 @@
 // adds the pieces in CTA order (the result does not depend on timing) and
 // stores y.  For a small epoch, where that final combine would cost more
 // than the imbalance, the range boundaries move back to row-block starts
-// instead (choose_aligned).  A launch takes up to 96 jobs (their tensor maps
-// travel in the kernel parameters); longer lists take several launches.
+// instead (choose_aligned).  A launch takes up to 96 jobs, 48 of them Q6_K
+// (their tensor maps travel in the kernel parameters); longer lists take
+// several launches.
+//
+// Q6_K jobs (GPU layout) are units of 32 rows x 2 superblocks of 208 bytes
+// plus the rows' d values (a second tensor copy); a segment holds one format,
+// and a launch that holds a Q6_K job sizes every ring slot for its units.
 //
 // Reduction.  Consumer warps take the CTA's units round-robin; each unit
 // leaves one partial per row in shared memory, and after a pass of units the
@@ -64,7 +69,15 @@ constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;          // + one producer warp
 constexpr int kRB = 32;                            // rows per block (one per lane)
 constexpr int kUnitSB = 2;                         // superblocks per unit
-constexpr int kUnitBytes = kUnitSB * kRB * kBlockBytes;   // one ring slot
+constexpr int kUnitBytes = kUnitSB * kRB * kBlockBytes;   // one ring slot (Q4_K units)
+// Q6_K units (GPU layout): 32 rows x 2 superblocks of 208 bytes, then the
+// rows' d values (an aligned group of 8 per row); a launch that holds a
+// Q6_K job uses slots of this size for all its units
+constexpr int kQ6UnitQuant = kUnitSB * kRB * gemv::kQ6Blk;
+constexpr int kQ6UnitBytes = kQ6UnitQuant + kRB * 16;
+constexpr int kLaunchQ6 = 48;                      // Q6_K jobs per launch (their d maps in the parameters)
+constexpr int kFmtQ4K = 0, kFmtQ6K = 1;
+static_assert(kQ6UnitQuant % 128 == 0 && kQ6UnitBytes % 128 == 0, "tensor-copy destinations 128-byte aligned");
 constexpr int kMaxRing = 24;
 constexpr int kLaunchJobs = 96;                    // jobs per launch (tensor maps in the parameters)
 constexpr size_t kSyncBytes = 256;
@@ -74,6 +87,7 @@ struct SeqJob {
   float* y;
   int rows;
   int rb_base;      // first row block of the job within its segment
+  int dmap;         // Q6_K: index of the d-value map, else -1
 };
 
 struct SeqSeg {
@@ -83,6 +97,7 @@ struct SeqSeg {
   int nb;                // superblocks per row
   int nu;                // units per row block: ceil(nb / kUnitSB)
   int n_rb;              // row blocks of the segment
+  int fmt;               // weight format of its jobs (kFmtQ4K, kFmtQ6K)
 };
 
 struct SeqEpoch {
@@ -93,12 +108,14 @@ struct SeqEpoch {
 };
 
 struct SeqParams {
-  CUtensorMap map[kLaunchJobs];   // one per job: box of 144 bytes x 32 rows x 2 superblocks
+  CUtensorMap map[kLaunchJobs];   // one per job: box of 144 (Q6_K: 208) bytes x 32 rows x 2 superblocks
+  CUtensorMap dmap[kLaunchQ6];    // Q6_K jobs' d values: box of 8 x 32 rows
   SeqJob job[kLaunchJobs];
   SeqSeg seg[kLaunchJobs];
   SeqEpoch epoch[kLaunchJobs];
   int n_epoch;
   int ring;
+  int slot_bytes;     // kUnitBytes, or kQ6UnitBytes when the launch holds a Q6_K job
   int nb_max;
   int part_floats;
   unsigned* sync;     // [0] segment arrivals, [1] CTAs exited, [2] abort
@@ -114,7 +131,7 @@ struct SeqLayout {
   size_t xs, xss, part, carry, flags, ring, bars, total;
 };
 
-__host__ __device__ inline SeqLayout seq_layout(int B, int nb_max, int part_floats, int ring) {
+__host__ __device__ inline SeqLayout seq_layout(int B, int nb_max, int part_floats, int ring, int slot_bytes) {
   SeqLayout L;
   L.xs = 0;
   L.xss = L.xs + gemv::xs_bytes(B, nb_max);
@@ -122,7 +139,7 @@ __host__ __device__ inline SeqLayout seq_layout(int B, int nb_max, int part_floa
   L.carry = L.part + sizeof(float) * (size_t)part_floats;
   L.flags = L.carry + sizeof(float) * 2 * kRB * (size_t)B;
   L.ring = (L.flags + 16 + 127) & ~size_t(127);
-  L.bars = L.ring + (size_t)ring * kUnitBytes;
+  L.bars = L.ring + (size_t)ring * slot_bytes;
   L.total = L.bars + sizeof(uint64_t) * 2 * ring + 16 + 1024;   // + issue counter, + base alignment slack
   return L;
 }
@@ -216,7 +233,7 @@ __device__ __forceinline__ float* piece_of(const SeqParams& P, const SeqEpoch& E
 // Consumer warps over slots [ps, pe) of a run of one segment's units: slot s
 // is segment unit u0 + s and stage J + s.  Each unit leaves 32 partial row
 // sums (its two superblocks added in order) in part[s - ps][row][b].
-template <int B>
+template <int B, int FMT>
 __device__ __forceinline__ void consume_pass(const SeqParams& P, const uint8_t* ring_base, uint64_t* full,
                                              uint64_t* empty, volatile int* issued, int ring, int J, int ps,
                                              int pe, long long u0, int nb, int nu, const gemv::XView& xv,
@@ -240,13 +257,27 @@ __device__ __forceinline__ void consume_pass(const SeqParams& P, const uint8_t* 
     for (int b = 0; b < B; ++b) acc[b] = 0.0f;
     if (ok) {
       const int sb = (int)((u0 + s) % nu) * kUnitSB;
-      const uint8_t* p = ring_base + (size_t)slot * kUnitBytes + lane * kBlockBytes;
-      gemv::superblock_dot<B, 4, true>(p, xv, sb, 0, acc);
-      if (sb + 1 < nb) {
-        float acc2[B];
-        gemv::superblock_dot<B, 4, true>(p + kRB * kBlockBytes, xv, sb + 1, 0, acc2);
+      const uint8_t* slot_p = ring_base + (size_t)slot * P.slot_bytes;
+      if constexpr (FMT == kFmtQ6K) {
+        // [superblock][row][208], then d as [row][8] for the aligned group holding sb
+        const uint8_t* p = slot_p + lane * gemv::kQ6Blk;
+        const __half* dv = reinterpret_cast<const __half*>(slot_p + kQ6UnitQuant) + lane * 8 + (sb & 7);
+        gemv::superblock_dot_q6<B, 4, true>(p, __half2float(dv[0]), xv, sb, 0, acc);
+        if (sb + 1 < nb) {
+          float acc2[B];
+          gemv::superblock_dot_q6<B, 4, true>(p + kRB * gemv::kQ6Blk, __half2float(dv[1]), xv, sb + 1, 0, acc2);
 #pragma unroll
-        for (int b = 0; b < B; ++b) acc[b] += acc2[b];
+          for (int b = 0; b < B; ++b) acc[b] += acc2[b];
+        }
+      } else {
+        const uint8_t* p = slot_p + lane * kBlockBytes;
+        gemv::superblock_dot<B, 4, true>(p, xv, sb, 0, acc);
+        if (sb + 1 < nb) {
+          float acc2[B];
+          gemv::superblock_dot<B, 4, true>(p + kRB * kBlockBytes, xv, sb + 1, 0, acc2);
+#pragma unroll
+          for (int b = 0; b < B; ++b) acc[b] += acc2[b];
+        }
       }
     }
     __syncwarp();
@@ -298,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int ring = P.ring;
-  const SeqLayout L = seq_layout(B, P.nb_max, P.part_floats, ring);
+  const SeqLayout L = seq_layout(B, P.nb_max, P.part_floats, ring, P.slot_bytes);
   uint8_t* xs = smem + L.xs;
   float2* xss = reinterpret_cast<float2*>(smem + L.xss);
   float* part = reinterpret_cast<float*>(smem + L.part);
@@ -348,9 +379,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
               pok = false;
               break;
             }
-            tc::mbar_arrive_expect_tx(&full[slot], kUnitBytes);
-            tc::tma_load_3d(ring_base + (size_t)slot * kUnitBytes, &P.map[jb], 0,
-                            (int)(rb - P.job[jb].rb_base) * kRB, up * kUnitSB, &full[slot]);
+            uint8_t* dst = ring_base + (size_t)slot * P.slot_bytes;
+            const int row = (int)(rb - P.job[jb].rb_base) * kRB;
+            if (S.fmt == kFmtQ6K) {
+              tc::mbar_arrive_expect_tx(&full[slot], kQ6UnitBytes);
+              tc::tma_load_3d(dst, &P.map[jb], 0, row, up * kUnitSB, &full[slot]);
+              tc::tma_load_2d(dst + kQ6UnitQuant, &P.dmap[P.job[jb].dmap], (up * kUnitSB) & ~7, row, &full[slot]);
+            } else {
+              tc::mbar_arrive_expect_tx(&full[slot], kUnitBytes);
+              tc::tma_load_3d(dst, &P.map[jb], 0, row, up * kUnitSB, &full[slot]);
+            }
             __threadfence_block();
             *issued = ++j;
             if (++slot == ring) {
@@ -415,8 +453,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
       const int pu = P.part_floats / per;   // units per pass
       for (int ps = 0; ps < n_units; ps += pu, ++pass_no) {
         const int pe = min(ps + pu, n_units);
-        consume_pass<B>(P, ring_base, full, empty, issued, ring, J, ps, pe, u0, nb, nu,
-                        gemv::make_view(xs, xss, S.x, B, nb), part, ok, warp, lane);
+        if (S.fmt == kFmtQ6K)
+          consume_pass<B, kFmtQ6K>(P, ring_base, full, empty, issued, ring, J, ps, pe, u0, nb, nu,
+                                   gemv::make_view(xs, xss, S.x, B, nb), part, ok, warp, lane);
+        else
+          consume_pass<B, kFmtQ4K>(P, ring_base, full, empty, issued, ring, J, ps, pe, u0, nb, nu,
+                                   gemv::make_view(xs, xss, S.x, B, nb), part, ok, warp, lane);
         if (!ok) flags[2] = 1;
         named_sync_consumers();
         ok = ok && !flags[2];
@@ -542,15 +584,20 @@ int plan_launch(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& i
   SeqEpoch tep[kLaunchJobs];
   const void* tw[kLaunchJobs];
   int64_t tcols[kLaunchJobs];
+  int tfmt[kLaunchJobs];
+  int n_q6 = 0;
   bool pending_wait = false;
   const float* cur_x = nullptr;
-  int cur_nb = -1;
+  int cur_nb = -1, cur_fmt = -1;
   for (int i = 0; i < n_jobs; ++i) {
     const q4k_gemv_job& q = jobs[i];
     pending_wait = pending_wait || q.wait != 0;
     if (q.rows == 0) continue;
     const int nb = (int)(q.cols / kQK);
-    if (n_seg == 0 || pending_wait || q.x != cur_x || nb != cur_nb) {
+    const int fmt = q.format == 1 ? kFmtQ6K : kFmtQ4K;
+    // a segment holds one weight format (same x across a format change:
+    // the next segment does not stage x again)
+    if (n_seg == 0 || pending_wait || q.x != cur_x || nb != cur_nb || fmt != cur_fmt) {
       if (n_seg > 0) tseg[n_seg - 1].job_end = n_job;
       if (n_seg == 0 || pending_wait) {
         if (n_epoch > 0) tep[n_epoch - 1].seg_end = n_seg;
@@ -562,17 +609,25 @@ int plan_launch(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& i
       sg.x = q.x;
       sg.job_begin = n_job;
       sg.nb = nb;
+      sg.fmt = fmt;
       tseg[n_seg++] = sg;
       cur_x = q.x;
       cur_nb = nb;
+      cur_fmt = fmt;
       pending_wait = false;
     }
     SeqJob jb{};
     jb.res = q.residual;
     jb.y = q.y;
     jb.rows = (int)q.rows;
+    jb.dmap = -1;
+    if (fmt == kFmtQ6K) {
+      if (n_q6 == kLaunchQ6) return Q4K_ERR_UNSUPPORTED;   // (the chunking keeps launches below this)
+      jb.dmap = n_q6++;
+    }
     tw[n_job] = q.w;
     tcols[n_job] = q.cols;
+    tfmt[n_job] = fmt;
     tjob[n_job++] = jb;
   }
   if (n_seg > 0) tseg[n_seg - 1].job_end = n_job;
@@ -604,8 +659,9 @@ int plan_launch(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& i
   // shared memory: activations, partial sums, then the deepest ring that fits
   p.part_floats = 16 * kRB * B * (B == 1 ? 16 : (B == 2 ? 8 : (B <= 4 ? 2 : 1)));
   p.ring = 0;
+  const int slot_bytes = n_q6 > 0 ? kQ6UnitBytes : kUnitBytes;
   for (int ring = kMaxRing; ring >= 4; --ring) {
-    const size_t total = seq_layout(B, p.nb_max, p.part_floats, ring).total;
+    const size_t total = seq_layout(B, p.nb_max, p.part_floats, ring, slot_bytes).total;
     if (total <= (size_t)info.max_smem_optin) {
       p.ring = ring;
       p.smem = total;
@@ -620,19 +676,28 @@ int plan_launch(const q4k_gemv_job* jobs, int n_jobs, int B, const DeviceInfo& i
   p.ws_bytes = p.pieces_off + sizeof(float) * 2 * (size_t)p.grid * 2 * kRB * B;
   if (P) {
     for (int j = 0; j < n_job; ++j) {
-      // box: a superblock's 144 bytes x 32 rows x 2 superblocks; rows and
-      // superblocks past the matrix read as zeros
+      // box: a superblock's 144 (Q6_K: 208) bytes x 32 rows x 2 superblocks;
+      // rows and superblocks past the matrix read as zeros
       const uint64_t nbj = (uint64_t)(tcols[j] / kQK);
-      const uint64_t dims[3] = {(uint64_t)kBlockBytes, (uint64_t)tjob[j].rows, nbj};
-      const uint64_t strides[2] = {nbj * kBlockBytes, (uint64_t)kBlockBytes};
-      const uint32_t box[3] = {(uint32_t)kBlockBytes, (uint32_t)kRB, (uint32_t)kUnitSB};
+      const bool q6 = tfmt[j] == kFmtQ6K;
+      const uint64_t blk = q6 ? (uint64_t)gemv::kQ6Blk : (uint64_t)kBlockBytes;
+      const uint64_t row_bytes = q6 ? (uint64_t)q6k_gpu_row_bytes((int64_t)nbj) : nbj * kBlockBytes;
+      const uint64_t dims[3] = {blk, (uint64_t)tjob[j].rows, nbj};
+      const uint64_t strides[2] = {row_bytes, blk};
+      const uint32_t box[3] = {(uint32_t)blk, (uint32_t)kRB, (uint32_t)kUnitSB};
       if (!encode_tmap_u8_3d(&P->map[j], tw[j], dims, strides, box)) return Q4K_ERR_CUDA;
+      // Q6_K: the rows' d values after their superblocks, 8 x 32 rows a box
+      if (q6 && !encode_tmap_2d(&P->dmap[tjob[j].dmap], CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                                static_cast<const uint8_t*>(tw[j]) + nbj * blk, nbj, (uint64_t)tjob[j].rows,
+                                row_bytes, 8, (uint32_t)kRB, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return Q4K_ERR_CUDA;
     }
     std::memcpy(P->seg, tseg, sizeof(SeqSeg) * n_seg);
     std::memcpy(P->job, tjob, sizeof(SeqJob) * n_job);
     std::memcpy(P->epoch, tep, sizeof(SeqEpoch) * n_epoch);
     P->n_epoch = n_epoch;
     P->ring = p.ring;
+    P->slot_bytes = slot_bytes;
     P->nb_max = p.nb_max;
     P->part_floats = p.part_floats;
   }
@@ -699,9 +764,21 @@ cudaError_t launch_seq_batch(const SeqParams& P, const SeqPlan& p, int batch, cu
 }
 
 // Launches of a job list: consecutive chunks of at most kLaunchJobs jobs
-// (stream order between launches is a full dependency).
-int next_chunk(int i0, int n_jobs) { return std::min(n_jobs, i0 + kLaunchJobs); }
-int n_launches(int n_jobs) { return n_jobs <= 0 ? 1 : (n_jobs + kLaunchJobs - 1) / kLaunchJobs; }
+// (stream order between launches is a full dependency), each holding at most
+// kLaunchQ6 Q6_K jobs with work
+int next_chunk(const q4k_gemv_job* jobs, int i0, int n_jobs) {
+  int i = i0, q6 = 0;
+  while (i < n_jobs && i - i0 < kLaunchJobs) {
+    if (jobs[i].format == 1 && jobs[i].rows > 0) {
+      if (q6 == kLaunchQ6) break;
+      ++q6;
+    }
+    ++i;
+  }
+  return i;
+}
+// an upper bound on the launches of any list of n_jobs jobs (plan buffers)
+int n_launches(int n_jobs) { return n_jobs <= 0 ? 1 : (n_jobs + kLaunchQ6 - 1) / kLaunchQ6; }
 
 // A prepared job list in caller-owned host memory: a header, then one
 // (kernel parameters, launch shape) pair per launch.
@@ -746,10 +823,10 @@ int build_plan(const q4k_gemv_job* jobs, int n_jobs, int batch, void* buf, size_
   h->magic = 0;
   size_t need = kSyncBytes;
   int k = 0;
-  for (int i0 = 0; i0 < n_jobs || k == 0; i0 = next_chunk(i0, n_jobs), ++k) {
+  for (int i0 = 0; i0 < n_jobs || k == 0; i0 = next_chunk(jobs, i0, n_jobs), ++k) {
     SeqLaunch& l = L[k];
     std::memset(&l.P, 0, sizeof(l.P));
-    const int st = plan_launch(jobs + i0, next_chunk(i0, n_jobs) - i0, batch, info, &l.P, &l.plan);
+    const int st = plan_launch(jobs + i0, next_chunk(jobs, i0, n_jobs) - i0, batch, info, &l.P, &l.plan);
     if (st == Q4K_ERR_CUDA) *ce = cudaErrorInvalidValue;   // a tensor map the driver refused
     if (st != Q4K_OK) return st;
     l.active = l.plan.n_epoch > 0;
@@ -803,7 +880,8 @@ int run_plan(const void* buf, cudaStream_t s, cudaError_t* ce) {
 // Per-thread plan buffer of the one-shot entry points (a job list of the
 // maximum length takes three launches).
 struct alignas(64) OneShotPlan {
-  uint8_t bytes[sizeof(PlanHeader) + sizeof(SeqLaunch) * ((kGemvSeqMaxJobs + kLaunchJobs - 1) / kLaunchJobs)];
+  // room for the most launches any list can take (n_launches(kGemvSeqMaxJobs))
+  uint8_t bytes[sizeof(PlanHeader) + sizeof(SeqLaunch) * ((kGemvSeqMaxJobs + kLaunchQ6 - 1) / kLaunchQ6)];
 };
 OneShotPlan* one_shot_plan() {
   static thread_local OneShotPlan* p = new OneShotPlan;
@@ -817,9 +895,9 @@ int gemv_seq_workspace(const q4k_gemv_job* jobs, int n_jobs, int batch, size_t* 
   if (cudaGetDevice(&dev) != cudaSuccess) return Q4K_ERR_CUDA;
   const DeviceInfo& info = device_info(dev);
   size_t need = kSyncBytes;
-  for (int i0 = 0; i0 < n_jobs; i0 = next_chunk(i0, n_jobs)) {
+  for (int i0 = 0; i0 < n_jobs; i0 = next_chunk(jobs, i0, n_jobs)) {
     SeqPlan p;
-    const int st = plan_launch(jobs + i0, next_chunk(i0, n_jobs) - i0, batch, info, nullptr, &p);
+    const int st = plan_launch(jobs + i0, next_chunk(jobs, i0, n_jobs) - i0, batch, info, nullptr, &p);
     if (st != Q4K_OK) return st;
     need = std::max(need, p.ws_bytes);
   }

@@ -154,8 +154,9 @@ def test_gemv_seq_plan_validates_like_the_one_shot_call(lib):
         return arr
 
     n1 = lib.q4k_gemv_seq_plan_bytes(1)
-    assert n1 > 0 and lib.q4k_gemv_seq_plan_bytes(96) == n1              # one launch holds 96 jobs
-    assert lib.q4k_gemv_seq_plan_bytes(97) > n1
+    # room for one launch per 48 jobs: a list may hold up to 48 Q6_K jobs a launch
+    assert n1 > 0 and lib.q4k_gemv_seq_plan_bytes(48) == n1
+    assert lib.q4k_gemv_seq_plan_bytes(49) > n1
     assert lib.q4k_gemv_seq_plan_bytes(256) > lib.q4k_gemv_seq_plan_bytes(97)
     assert lib.q4k_gemv_seq_plan_bytes(257) == 0 and lib.q4k_gemv_seq_plan_bytes(-1) == 0
     raw = ctypes.create_string_buffer(n1 + 128)
@@ -223,6 +224,9 @@ def test_gemv_seq_validation_before_any_launch(lib):
     assert lib.q4k_gemv_seq(ok2, -1, 0, 1, ws, 1 << 20, None) == 1
     assert lib.q4k_gemv_seq(jobs(*[(8, 256, fake)] * 257), 257, 0, 1, ws, 1 << 20, None) == 3
     assert lib.q4k_gemv_seq(ok2, 2, 5, 1, ws, 1 << 20, None) == 3            # unknown layout
+    bad_fmt = jobs((8, 256, fake))
+    bad_fmt[0].format = 2                                                     # neither Q4_K nor Q6_K
+    assert lib.q4k_gemv_seq(bad_fmt, 1, 0, 1, ws, 1 << 20, None) == 1
     assert lib.q4k_gemv_seq(ok2, 2, 0, 9, ws, 1 << 20, None) == 3            # batch above 8
     assert lib.q4k_gemv_seq(ok2, 2, 0, -1, ws, 1 << 20, None) == 1
     assert lib.q4k_gemv_seq(jobs((8, 300, fake)), 1, 0, 1, ws, 1 << 20, None) == 1

@@ -252,3 +252,93 @@ def test_plan_and_one_shot_call_give_the_same_bits():
     torch.cuda.synchronize()
     for n in SHAPES:
         assert torch.equal(y1[n], y2[n]), n
+
+
+# ------------------------------------------------------- Q4_K_M job lists
+Q6K_IN_LAYER = ("v", "down")     # the Q6_K matrices of a Q4_K_M layer (half the layers)
+
+
+def q6_pack(f):
+    return q4k.q6k_pack(dev(np.ascontiguousarray(f["d"]).view(np.int16)), dev(f["sc"]), dev(f["q"]))
+
+
+def q4km_layer(seed, batch):
+    """A Q4_K_M-style decode layer: q, k, o, gate, up in Q4_K; v, down in Q6_K."""
+    from oracle import q6k as O6
+    fields, xs = synth.decode_layer(synth.WL_DECODE_4B, seed, batch)
+    w, ref_f = {}, {}
+    for n, (rows, cols, _) in SHAPES.items():
+        if n in Q6K_IN_LAYER:
+            f6 = synth.q6k_fields(rows, cols, [790, seed, rows])
+            w[n], ref_f[n] = q6_pack(f6), ("q6", f6)
+        else:
+            w[n], ref_f[n] = pack_dev(fields[n]), ("q4", fields[n])
+
+    def ref(n, x, r=None):
+        kind, f = ref_f[n]
+        return O6.gemv_q6k(f, x, r) if kind == "q6" else O.gemv(f, x, r)
+    return w, xs, ref
+
+
+def q4km_jobs(w, xs_dev, ys, residuals=None):
+    jobs = layer_jobs(w, xs_dev, ys, None, residuals)
+    for j, (n, _) in zip(jobs, [(n, 0) for names in GROUPS for n in names]):
+        if n in Q6K_IN_LAYER:
+            j["format"] = 1
+    return jobs
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_q4km_layer_mixed_formats(batch):
+    """q, k (Q4_K) and v (Q6_K) read the same x: two segments, one staging;
+    down (Q6_K) waits and adds the residual."""
+    w, xs, ref = q4km_layer(3, batch)
+    xs_dev = {k: dev(v) for k, v in xs.items()}
+    ys = {n: torch.full((batch, SHAPES[n][0]), float("nan"), device="cuda") for n in SHAPES}
+    r = synth.residual(batch, SHAPES["down"][0], [791, batch])
+    q4k.q4k_gemv_seq(q4km_jobs(w, xs_dev, ys, {"down": dev(r)}), batch)
+    for n, (rows, cols, inp) in SHAPES.items():
+        assert_close(host(ys[n]), *ref(n, xs[inp], r if n == "down" else None), f"{n} (batch {batch})")
+    assert q4k.q4k_device_error() == 0
+
+
+def test_q4km_stack_across_launches_and_entry_points():
+    """Six Q4_K_M layers (42 jobs, 12 of them Q6_K) as one list through the
+    one-shot call, the prepared plan and the allocation-free entry: the same
+    bits from all three, within the bound.  A list of 60 Q6_K jobs takes two
+    launches (48 Q6_K jobs a launch)."""
+    batch = 1
+    layers = [q4km_layer(10 + i, batch) for i in range(6)]
+    jobs, checks = [], []
+    for w, xs, ref in layers:
+        xs_dev = {k: dev(v) for k, v in xs.items()}
+        ys = {n: torch.full((batch, SHAPES[n][0]), float("nan"), device="cuda") for n in SHAPES}
+        jobs += q4km_jobs(w, xs_dev, ys)
+        checks.append((xs, ref, ys))
+    q4k.q4k_gemv_seq(jobs, batch)
+    first = {id(c): {n: host(c[2][n]).copy() for n in SHAPES} for c in checks}
+    for xs, ref, ys in checks:
+        for n, (rows, cols, inp) in SHAPES.items():
+            assert_close(host(ys[n]), *ref(n, xs[inp]), n)
+    seq = q4k.GemvSeq(jobs, batch)
+    seq()
+    for c in checks:
+        for n in SHAPES:
+            assert np.array_equal(host(c[2][n]), first[id(c)][n]), f"plan: {n}"
+    q4k.q4k_gemv_seq_static(jobs, batch)
+    for c in checks:
+        for n in SHAPES:
+            assert np.array_equal(host(c[2][n]), first[id(c)][n]), f"static: {n}"
+    # 60 Q6_K jobs (small): two launches
+    from oracle import q6k as O6
+    cols = 512
+    x = synth.activations(batch, cols, 792)
+    xd = dev(x)
+    fs = [synth.q6k_fields(40 + (i % 5) * 16, cols, [793, i]) for i in range(60)]
+    ys6 = [torch.full((batch, f["q"].shape[0]), float("nan"), device="cuda") for f in fs]
+    jobs6 = [{"w": q6_pack(f), "rows": f["q"].shape[0], "cols": cols, "x": xd, "y": y, "format": 1,
+              "wait": i == 50} for i, (f, y) in enumerate(zip(fs, ys6))]
+    q4k.q4k_gemv_seq(jobs6, batch)
+    for i in (0, 47, 48, 50, 59):
+        assert_close(host(ys6[i]), *O6.gemv_q6k(fs[i], x), f"q6k job {i}")
+    assert q4k.q4k_device_error() == 0

@@ -507,6 +507,48 @@ def run_ours(args, rank, world):
     token_engine = {f"batch{b}": stack_token(b, True) for b in (1, 4)}
     stack_indep = {f"batch{b}": stack_token(b, False) for b in (1, 4)}
 
+    # Q4_K_M-style stack: v and down in Q6_K (GPU layout) in every other layer,
+    # one token in engine order through the job list (mixed formats)
+    q6_mats = {}
+    for n in ("v", "down"):
+        rows, cols, _ = shape[n]
+        f6 = synth.q6k_fields(rows, cols, [795, rows])
+        q6w = q4k.q6k_pack(torch.from_numpy(f6["d"].view(np.int16)).to(dev), torch.from_numpy(f6["sc"]).to(dev),
+                           torch.from_numpy(f6["q"]).to(dev))
+        q6_mats[n] = [q6w] + [q6w.clone() for _ in range(n_copies - 1)]
+        del f6
+
+    def q4km_token():
+        batch = 1
+        xs_b = {name: torch.from_numpy(synth.activations(batch, cols, synth.layer_seed(synth.WL_STACK_4B, 0, 200 + j)))
+                .to(dev) for j, (name, cols) in enumerate(synth.QWEN3_4B_INPUTS)}
+        ys_b = {n: torch.empty((batch, shape[n][0]), device=dev) for n in shape}
+        jobs, nbytes = [], 0
+        for L in range(36):
+            lj = layer_jobs(copies[L % n_copies], True, xs_b, ys_b)
+            lj[0]["wait"] = L > 0
+            for j in lj:
+                name = next(n for n in shape if ys_b[n] is j["y"])
+                rows, cols, _ = shape[name]
+                if L % 2 == 0 and name in q6_mats:
+                    j["w"], j["format"] = q6_mats[name][L % n_copies], 1
+                    nbytes += rows * (cols // 256) * 210
+                else:
+                    nbytes += rows * (cols // 256) * 144
+                nbytes += batch * (rows + cols) * 4
+            jobs += lj
+        tok = gemv_seq(jobs, batch)
+        tok()
+        torch.cuda.synchronize()
+        n_tok = 10
+        ms = time_graph(capture(lambda: [tok() for _ in range(n_tok)]), 10) / n_tok
+        return {"tokens_per_s": batch / (ms * 1e-3), "ms_per_token": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+                "weight_bytes": nbytes,
+                "note": "36 layers in engine order, v and down in Q6_K in layers 0, 2, ..., 34 (252 jobs)"}
+
+    token_q4km = q4km_token()
+    del q6_mats
+
     def q8_layers(batch, n_layers=20):
         """Decode layers at `batch` tokens through the q8_1 GEMV (MMQ form): per
         layer q8_1 of the four inputs and one q4k_gemv_q8 launch per matrix."""
@@ -758,7 +800,7 @@ def run_ours(args, rank, world):
     # launch duration is the replay over its launches, and each launch
     # processes its sets' algorithmic bytes
     achieved = step_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
-    traffic_rec = profile_traffic("gemv_seq", ["gemv_seq.cu", "gemv_common.cuh"])
+    traffic_rec = profile_traffic("gemv_seq", ["gemv_seq_kernel.cuh", "gemv_common.cuh"])
     traffic = None
     if traffic_rec is not None:
         # the record is for a launch of MAX_SETS_PER_LAUNCH sets: scale to this run's average launch
@@ -810,7 +852,8 @@ def run_ours(args, rank, world):
                                  "GB/s": step_bytes * args.steps / (ms_4launch * 1e-3) / 1e9},
             "layer_gemv_seq_with_waits": {"us_per_layer": 1e3 * ms_chain / args.steps,
                                           "GB/s": step_bytes * args.steps / (ms_chain * 1e-3) / 1e9},
-            "token_36_layers_gemv_seq_with_waits": token_engine},
+            "token_36_layers_gemv_seq_with_waits": token_engine,
+            "token_36_layers_q4_k_m_mixed_formats_batch1": token_q4km},
         "decode_q8_1_gemv_per_layer": q8_decode,
         "decode_q6k_gemv": {**q6k_decode,
                             "note": "q6k_gemv launches (fp32 activations) or q6k_gemm (q8_1 activations, one "

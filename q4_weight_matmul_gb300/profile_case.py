@@ -8,6 +8,7 @@
     python -m q4_weight_matmul_gb300.profile_case seq --layers 13 --batch 1 --reps 3
     python -m q4_weight_matmul_gb300.profile_case q6k_gemv --rows 151936 --cols 2560 --batch 1 --reps 3
     python -m q4_weight_matmul_gb300.profile_case gemm_f16 --rows 9728 --cols 2560 --tokens 512
+    python -m q4_weight_matmul_gb300.profile_case q6k_gemm_f16 --rows 2560 --cols 9728 --tokens 512
 
 ``seq`` runs --layers Qwen3-4B-shaped decode linear sets (q, k, v, o, gate,
 up, down; independent inputs) as one q4k_gemv_seq launch per rep, as the
@@ -60,7 +61,8 @@ def run_seq(a, dev, gen):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["gemv", "gemm", "gemm_h16", "gemm_f16", "q8", "pack", "seq", "q6k_gemv"])
+    ap.add_argument("kernel", choices=["gemv", "gemm", "gemm_h16", "gemm_f16", "q8", "pack", "seq", "q6k_gemv",
+                                       "q6k_gemm_f16"])
     ap.add_argument("--layers", type=int, default=13)
     ap.add_argument("--rows", type=int, default=9728)
     ap.add_argument("--cols", type=int, default=2560)
@@ -76,7 +78,7 @@ def main():
         run_seq(a, dev, gen)
         return
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
-    if a.kernel == "q6k_gemv":
+    if a.kernel in ("q6k_gemv", "q6k_gemm_f16"):
         d = (torch.rand((a.rows, a.cols // 256), generator=gen, device=dev) * 0.02).half().view(torch.int16)
         sc = torch.randint(-128, 128, (a.rows, a.cols // 16), generator=gen, device=dev,
                            dtype=torch.int16).to(torch.int8)
@@ -84,10 +86,16 @@ def main():
         w0 = q4k.q6k_pack(d, sc, q)
         n = max(1, math.ceil(2 * l2 / w0.numel()))
         ws = [w0] + [w0.clone() for _ in range(n - 1)]
-        x = torch.randn((a.batch, a.cols), device=dev, generator=gen)
-        y = torch.empty((a.batch, a.rows), device=dev)
-        for i in range(a.reps):
-            q4k.q6k_gemv(ws[i % n], a.rows, a.cols, x, y=y)
+        if a.kernel == "q6k_gemv":
+            x = torch.randn((a.batch, a.cols), device=dev, generator=gen)
+            y = torch.empty((a.batch, a.rows), device=dev)
+            for i in range(a.reps):
+                q4k.q6k_gemv(ws[i % n], a.rows, a.cols, x, y=y)
+        else:
+            sp = q4k.x_split_f16(torch.randn((a.tokens, a.cols), device=dev, generator=gen))
+            y = torch.empty((a.tokens, a.rows), device=dev)
+            for i in range(a.reps):
+                q4k.q6k_gemm_f16(ws[i % n], a.rows, a.cols, *sp, y=y)
         torch.cuda.synchronize()
         print("profile case done:", a.kernel, a.rows, a.cols, a.batch, a.reps)
         return

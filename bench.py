@@ -650,20 +650,31 @@ def run_ours(args, rank, world):
     e2e_calls = seq_calls(0, args.warmup + args.steps, max_per=1, xs_=xe, ys_=ye)
 
     def e2e_step(i):
+        # one C-ABI call: input copy, the planned launch, output copy
+        e2e_calls[i].launch_host(x_host, x_dev, y_host, y_dev)
+
+    def e2e_step_torch(i):
+        # the same step with the copies issued by torch around q4k_gemv_seq_launch
         x_dev.copy_(x_host, non_blocking=True)
-        e2e_calls[i]()   # one planned q4k_gemv_seq launch per step through the public API
+        e2e_calls[i]()
         y_host.copy_(y_dev, non_blocking=True)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    barrier()
-    e0, e1 = ev(), ev()
-    e0.record()
-    for i in range(args.steps):
-        e2e_step(args.warmup + i)
-    e1.record()
-    barrier()
-    e2e_ms = e0.elapsed_time(e1)
+    def e2e_time(step):
+        for i in range(args.warmup):
+            step(i)
+        barrier()
+        e0, e1 = ev(), ev()
+        t0 = time.perf_counter()
+        e0.record()
+        for i in range(args.steps):
+            step(args.warmup + i)
+        e1.record()
+        t1 = time.perf_counter()
+        barrier()
+        return e0.elapsed_time(e1), 1e6 * (t1 - t0) / args.steps
+
+    e2e_torch_ms, e2e_torch_host_us = e2e_time(e2e_step_torch)
+    e2e_ms, e2e_host_us = e2e_time(e2e_step)
 
     # ---------------- prefill GEMMs (q8_1 + MMQ)
     def prefill_case(mats, xs_in, tokens, layers=1, rotate=True, form="h16"):
@@ -788,6 +799,7 @@ def run_ours(args, rank, world):
 
     elapsed_ms = max_over_ranks(elapsed_ms)
     e2e_ms = max_over_ranks(e2e_ms)
+    e2e_torch_ms = max_over_ranks(e2e_torch_ms)
 
     if rank != 0:
         if dist is not None:
@@ -796,6 +808,7 @@ def run_ours(args, rank, world):
 
     value = job_throughput(step_bytes, args.steps, world, elapsed_ms)
     e2e_value = job_throughput(step_bytes, args.steps, world, e2e_ms)
+    e2e_torch_value = job_throughput(step_bytes, args.steps, world, e2e_torch_ms)
     # the timed replay holds nothing but this kernel's launches: the average
     # launch duration is the replay over its launches, and each launch
     # processes its sets' algorithmic bytes
@@ -836,13 +849,17 @@ def run_ours(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
                      "traffic": traffic, "peak_kind": f"{peak_kind} hbm_gbs",
-                     "kernel": "gemv_seq_kernel<1>",
+                     "kernel": "gemv_seq_kernel<1, 0>",
                      "duration": "CUDA events on the launching stream around each replay (one graph of the "
                                  "launches of this kernel, nothing else), divided by its launches; algorithmic "
                                  "bytes per launch = the sets it holds x bytes per set"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "per step: one copy of the 4 input vectors from pinned host memory, one q4k_gemv_seq_launch "
-                        "of a prepared plan, one copy of the 7 outputs back to pinned host memory; no graph"},
+                "us_per_step": 1e3 * e2e_ms / args.steps, "host_issue_us_per_step": e2e_host_us,
+                "torch_copies": {"value": e2e_torch_value, "us_per_step": 1e3 * e2e_torch_ms / args.steps,
+                                 "host_issue_us_per_step": e2e_torch_host_us},
+                "note": "per step one q4k_gemv_seq_launch_host call: a copy of the 4 input vectors from pinned "
+                        "host memory, the prepared plan's launch, a copy of the 7 outputs back to pinned host "
+                        "memory; no graph.  torch_copies: the same step with the copies issued by torch"},
         "gpu_launches": n_launch,
         "clocks": clocks,
         "time_x_sm_mhz": (elapsed_ms / args.steps * 1e3 * sm_mhz) if sm_mhz else None,

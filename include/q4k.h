@@ -300,6 +300,25 @@ int q4k_gemv_seq_plan(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t 
 int q4k_gemv_seq_launch(const void* plan, void* stream);
 
 /*
+ * q4k_gemv_seq_launch_host - one decode step from HOST buffers: enqueues on
+ * `stream`, in order, the copy of x_bytes bytes from x_host to x_dev, the
+ * plan's launches (as q4k_gemv_seq_launch) and the copy of y_bytes bytes
+ * from y_dev to y_host, and returns without waiting; y_host holds the
+ * step's outputs once the stream has reached that point (synchronise the
+ * stream before reading it).  x_dev and y_dev are device buffers that the
+ * caller laid out to hold the jobs' inputs and outputs (the plan's x and y
+ * pointers are views into them); the library cannot check that.  Host
+ * buffers should be pinned (page-locked), or the copies are not
+ * asynchronous.  A zero byte count skips that copy.
+ * Errors: Q4K_ERR_INVALID_ARG (null plan, or a null pointer with a non-zero
+ * byte count, or a plan made on another device) with nothing enqueued;
+ * Q4K_ERR_CUDA if an enqueue fails, after which the steps before it stay
+ * enqueued.
+ */
+int q4k_gemv_seq_launch_host(const void* plan, const void* x_host, void* x_dev, size_t x_bytes,
+                             void* y_host, const void* y_dev, size_t y_bytes, void* stream);
+
+/*
  * q4k_gemv_seq_static - q4k_gemv_seq for callers that cannot allocate device
  * memory: a serving process that fixes its device memory at start-up and may
  * not allocate afterwards, a plug-in that runs inside a host program whose

@@ -53,6 +53,7 @@ SIGNATURES = {
     "q4k_gemv_seq_plan_bytes": (ctypes.c_size_t, [_I]),
     "q4k_gemv_seq_plan": (_I, [_P, _I, _I, _I64, _P, ctypes.c_size_t, _P, ctypes.c_size_t]),
     "q4k_gemv_seq_launch": (_I, [_P, _P]),
+    "q4k_gemv_seq_launch_host": (_I, [_P, _P, _P, ctypes.c_size_t, _P, _P, ctypes.c_size_t, _P]),
     "q4k_gemv_seq_static": (_I, [_P, _I, _I, _I64, _P]),
     "q4k_gemm": (_I, [_P, _I, _I64, _I64, _P, _P, _P, _I64, _P, _P]),
     "q4k_gemm_blockdots": (_I, [_P, _I, _I64, _I64, _P, _I64, _P, _P]),
@@ -419,6 +420,30 @@ class GemvSeq:
 
     def __call__(self, stream=None):
         _check(lib().q4k_gemv_seq_launch(self.plan, _stream(stream)), "q4k_gemv_seq_launch")
+
+    def launch_host(self, x_host, x_dev, y_host, y_dev, stream=None):
+        """One step from host buffers (``q4k_gemv_seq_launch_host``): copy
+        ``x_host`` into ``x_dev``, launch, copy ``y_dev`` into ``y_host``, all
+        enqueued on the stream.  The jobs' x and y must be views of ``x_dev``
+        and ``y_dev``; the host tensors should be pinned.  Synchronise the
+        stream before reading ``y_host``."""
+        def _host(t, name):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous host tensor")
+            return t.data_ptr(), t.numel() * t.element_size()
+
+        def _dev(t, name, nbytes):
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous device tensor")
+            if t.numel() * t.element_size() < nbytes:
+                raise ValueError(f"{name} is smaller than its host buffer")
+            return t.data_ptr()
+
+        xh, xb = _host(x_host, "x_host")
+        yh, yb = _host(y_host, "y_host")
+        _check(lib().q4k_gemv_seq_launch_host(self.plan, xh, _dev(x_dev, "x_dev", xb), xb, yh,
+                                              _dev(y_dev, "y_dev", yb), yb, _stream(stream)),
+               "q4k_gemv_seq_launch_host")
 
 
 def q4k_gemv_seq(jobs, batch: int, layout: int = BLOCK144, workspace=None, stream=None):

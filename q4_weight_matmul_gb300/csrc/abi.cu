@@ -618,6 +618,24 @@ int q4k_gemv_seq_launch(const void* plan, void* stream) {
   return st;
 }
 
+int q4k_gemv_seq_launch_host(const void* plan, const void* x_host, void* x_dev, size_t x_bytes, void* y_host,
+                             const void* y_dev, size_t y_bytes, void* stream) {
+  if (!plan) return Q4K_ERR_INVALID_ARG;
+  if (x_bytes && (!x_host || !x_dev)) return Q4K_ERR_INVALID_ARG;
+  if (y_bytes && (!y_host || !y_dev)) return Q4K_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t ce = cudaSuccess;
+  if (const int st = gemv_seq_check_plan(plan, &ce)) return st == Q4K_ERR_CUDA ? record_cuda(ce) : st;
+  if (x_bytes && (ce = cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return record_cuda(ce);
+  const int st = gemv_seq_launch(plan, s, &ce);
+  if (st == Q4K_ERR_CUDA) return record_cuda(ce);
+  if (st != Q4K_OK) return st;
+  if (y_bytes && (ce = cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return record_cuda(ce);
+  return Q4K_OK;
+}
+
 int q4k_gemv_seq_static(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t batch, void* stream) {
   bool work = false;
   if (int e = check_seq(jobs, n_jobs, layout, batch, &work)) return e;

@@ -333,13 +333,20 @@ int bind_workspace(void* buf, void* ws, size_t ws_bytes) {
   return Q4K_OK;
 }
 
-int run_plan(const void* buf, cudaStream_t s, cudaError_t* ce) {
+// Q4K_OK when `buf` holds a plan written by gemv_seq_plan on the current device.
+int check_plan(const void* buf, cudaError_t* ce) {
   *ce = cudaSuccess;
   const PlanHeader* h = static_cast<const PlanHeader*>(buf);
   if (h->magic != kPlanMagic || !h->ws) return Q4K_ERR_INVALID_ARG;
   int dev = 0;
   if ((*ce = cudaGetDevice(&dev)) != cudaSuccess) return Q4K_ERR_CUDA;
   if (dev != h->dev) return Q4K_ERR_INVALID_ARG;
+  return Q4K_OK;
+}
+
+int run_plan(const void* buf, cudaStream_t s, cudaError_t* ce) {
+  if (const int st = check_plan(buf, ce)) return st;
+  const PlanHeader* h = static_cast<const PlanHeader*>(buf);
   const SeqLaunch* L = reinterpret_cast<const SeqLaunch*>(static_cast<const uint8_t*>(buf) + sizeof(PlanHeader));
   for (int k = 0; k < h->n_launch; ++k) {
     if (!L[k].active) continue;
@@ -404,6 +411,8 @@ int gemv_seq_plan(const q4k_gemv_job* jobs, int n_jobs, int batch, void* workspa
 }
 
 int gemv_seq_launch(const void* plan, cudaStream_t s, cudaError_t* cuda_err) { return run_plan(plan, s, cuda_err); }
+
+int gemv_seq_check_plan(const void* plan, cudaError_t* cuda_err) { return check_plan(plan, cuda_err); }
 
 int launch_gemv_seq(const q4k_gemv_job* jobs, int n_jobs, int batch, void* workspace, size_t workspace_bytes,
                     cudaStream_t s, cudaError_t* cuda_err) {

@@ -88,6 +88,8 @@ size_t gemv_seq_plan_bytes(int n_jobs);
 int gemv_seq_plan(const q4k_gemv_job* jobs, int n_jobs, int batch, void* workspace, size_t workspace_bytes,
                   void* plan, size_t plan_bytes, cudaError_t* cuda_err);
 int gemv_seq_launch(const void* plan, cudaStream_t s, cudaError_t* cuda_err);
+// Q4K_OK when `plan` is a valid plan made on the current device (enqueues nothing).
+int gemv_seq_check_plan(const void* plan, cudaError_t* cuda_err);
 // The same with the library's built-in scratch array as the workspace.
 int launch_gemv_seq_static(const q4k_gemv_job* jobs, int n_jobs, int batch, cudaStream_t s,
                            cudaError_t* cuda_err);

@@ -172,6 +172,15 @@ def test_gemv_seq_plan_validates_like_the_one_shot_call(lib):
     assert lib.q4k_gemv_seq_plan(ok1, 1, 0, 1, None, 1 << 20, plan, n1) == 1          # no workspace
     assert lib.q4k_gemv_seq_plan(ok1, 1, 0, 1, ws, 1 << 20, None, n1) == 1            # no plan
     assert lib.q4k_gemv_seq_launch(None, None) == 1
+    # the host-buffer step checks its pointers and the plan before any copy
+    zeroed = ctypes.create_string_buffer(n1 + 128)
+    zplan = ctypes.addressof(zeroed) + (-ctypes.addressof(zeroed)) % 64
+    assert lib.q4k_gemv_seq_launch_host(None, fake, fake, 16, fake, fake, 16, None) == 1
+    assert lib.q4k_gemv_seq_launch_host(zplan, None, fake, 16, fake, fake, 16, None) == 1
+    assert lib.q4k_gemv_seq_launch_host(zplan, fake, None, 16, fake, fake, 16, None) == 1
+    assert lib.q4k_gemv_seq_launch_host(zplan, fake, fake, 16, None, fake, 16, None) == 1
+    assert lib.q4k_gemv_seq_launch_host(zplan, fake, fake, 16, fake, None, 16, None) == 1
+    assert lib.q4k_gemv_seq_launch_host(zplan, None, None, 0, None, None, 0, None) == 1   # not a plan
 
 
 def test_status_strings_and_version(lib):

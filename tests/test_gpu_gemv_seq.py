@@ -254,6 +254,50 @@ def test_plan_and_one_shot_call_give_the_same_bits():
         assert torch.equal(y1[n], y2[n]), n
 
 
+def test_host_buffer_step_matches_device_launch():
+    """q4k_gemv_seq_launch_host: inputs copied from one pinned host buffer,
+    outputs copied back into another, three steps with new host values;
+    each step gives the bits of the device-buffer launch on the same values
+    and matches the oracle on sampled rows."""
+    batch = 1
+    fields, xs = synth.decode_layer(synth.WL_DECODE_4B, 12, batch)
+    w = {n: pack_dev(fields[n]) for n in SHAPES}
+    in_off, off = {}, 0
+    for k, v in xs.items():
+        in_off[k] = (off, v.shape)
+        off += v.size
+    x_host = torch.empty(off, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty(off, device="cuda")
+    xv = {k: x_dev[o:o + int(np.prod(shp))].view(shp) for k, (o, shp) in in_off.items()}
+    y_off, off = {}, 0
+    for n in SHAPES:
+        y_off[n] = off
+        off += batch * SHAPES[n][0]
+    y_dev = torch.empty(off, device="cuda")
+    y_host = torch.full((off,), float("nan"), dtype=torch.float32).pin_memory()
+    yv = {n: y_dev[o:o + batch * SHAPES[n][0]].view(batch, SHAPES[n][0]) for n, o in y_off.items()}
+    seq = q4k.GemvSeq(layer_jobs(w, xv, yv, batch), batch)
+    xd = {k: torch.empty(v.shape, device="cuda") for k, v in xs.items()}
+    y2 = {n: torch.empty((batch, SHAPES[n][0]), device="cuda") for n in SHAPES}
+    ref = q4k.GemvSeq(layer_jobs(w, xd, y2, batch), batch)
+    rows = np.random.default_rng(13).choice(1024, 24, replace=False)
+    for step in range(3):
+        x_np = {k: synth.activations(batch, v.shape[1], [14, step, i]) for i, (k, v) in enumerate(xs.items())}
+        for k, (o, _) in in_off.items():
+            x_host[o:o + x_np[k].size] = torch.from_numpy(x_np[k].reshape(-1))
+            xd[k].copy_(torch.from_numpy(x_np[k]))
+        seq.launch_host(x_host, x_dev, y_host, y_dev)
+        ref()
+        torch.cuda.synchronize()
+        for n in SHAPES:
+            o, r = y_off[n], SHAPES[n][0]
+            got = y_host[o:o + batch * r].view(batch, r)
+            assert torch.equal(got, y2[n].cpu()), f"step {step} {n}: bits differ from the device launch"
+            y_ref, norm = O.gemv(slice_rows(fields[n], rows), x_np[SHAPES[n][2]])
+            assert_close(got.numpy()[:, rows], y_ref, norm, f"step {step} {n}")
+    assert q4k.q4k_device_error() == 0
+
+
 # ------------------------------------------------------- Q4_K_M job lists
 Q6K_IN_LAYER = ("v", "down")     # the Q6_K matrices of a Q4_K_M layer (half the layers)
 

@@ -300,7 +300,10 @@ int q4k_gemv_seq_plan(const q4k_gemv_job* jobs, int n_jobs, int layout, int64_t 
 int q4k_gemv_seq_launch(const void* plan, void* stream);
 
 /*
- * q4k_gemv_seq_launch_host - one decode step from HOST buffers: enqueues on
+ * q4k_gemv_seq_launch_host - one decode step from HOST buffers, for an
+ * engine whose activations live on the host between steps (the pages'
+ * engine keeps its buffers allocated for the whole run and only moves data
+ * on the hot path, genie-ai-runtime §4 "Memory-first"): enqueues on
  * `stream`, in order, the copy of x_bytes bytes from x_host to x_dev, the
  * plan's launches (as q4k_gemv_seq_launch) and the copy of y_bytes bytes
  * from y_dev to y_host, and returns without waiting; y_host holds the

@@ -630,8 +630,9 @@ def run_ours(args, rank, world):
     # Every step (decode set) has its own 4 input vectors and 7 outputs, rows
     # of one pinned host array each way.  The steps run in the headline's
     # launches (even split, at most MAX_SETS_PER_LAUNCH sets per launch), one
-    # q4k_gemv_seq_launch_host call per launch: the copy of its sets' inputs,
-    # the planned launch, the copy of its sets' outputs.
+    # q4k_gemv_seq_launch_host call per launch (GemvSeq.step on buffers bound
+    # before the timed region): the copy of its sets' inputs, the planned
+    # launch, the copy of its sets' outputs.
     in_off, off = {}, 0
     for k, v in xs_np.items():
         in_off[k] = (off, v.shape)
@@ -666,7 +667,8 @@ def run_ours(args, rank, world):
             for k in range(i, i + n):
                 jobs += layer_jobs(copies[k % n_copies], False, *set_views(k))
             seq = gemv_seq(jobs)
-            calls.append((seq, i, i + n))
+            seq.bind_host(x_host[i:i + n], x_dev[i:i + n], y_host[i:i + n], y_dev[i:i + n])
+            calls.append(seq)
             i += n
         return calls
 
@@ -676,14 +678,14 @@ def run_ours(args, rank, world):
     def e2e_time(max_per):
         warm = e2e_launches(0, args.warmup, max_per)
         timed = e2e_launches(args.warmup, args.steps, max_per)
-        for seq, i0, i1 in warm:
-            seq.launch_host(x_host[i0:i1], x_dev[i0:i1], y_host[i0:i1], y_dev[i0:i1])
+        for seq in warm:
+            seq.step()
         barrier()
         e0, e1 = ev(), ev()
         t0 = time.perf_counter()
         e0.record()
-        for seq, i0, i1 in timed:
-            seq.launch_host(x_host[i0:i1], x_dev[i0:i1], y_host[i0:i1], y_dev[i0:i1])
+        for seq in timed:
+            seq.step()
         e1.record()
         t1 = time.perf_counter()
         barrier()

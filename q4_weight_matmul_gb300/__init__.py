@@ -445,6 +445,25 @@ class GemvSeq:
                                               _dev(y_dev, "y_dev", yb), yb, _stream(stream)),
                "q4k_gemv_seq_launch_host")
 
+    def bind_host(self, x_host, x_dev, y_host, y_dev):
+        """Check the four buffers of ``launch_host`` once and keep them (and
+        references to them), so that ``step`` passes only pointers."""
+        for t, name, cuda in ((x_host, "x_host", False), (x_dev, "x_dev", True), (y_host, "y_host", False),
+                              (y_dev, "y_dev", True)):
+            if t.is_cuda != cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous {'device' if cuda else 'host'} tensor")
+        xb, yb = x_host.numel() * x_host.element_size(), y_host.numel() * y_host.element_size()
+        if x_dev.numel() * x_dev.element_size() < xb or y_dev.numel() * y_dev.element_size() < yb:
+            raise ValueError("a device buffer is smaller than its host buffer")
+        self._bound = (x_host, x_dev, y_host, y_dev)
+        self._bound_args = (x_host.data_ptr(), x_dev.data_ptr(), xb, y_host.data_ptr(), y_dev.data_ptr(), yb)
+
+    def step(self, stream=None):
+        """``launch_host`` on the buffers given to ``bind_host``."""
+        xh, xd, xb, yh, yd, yb = self._bound_args
+        _check(lib().q4k_gemv_seq_launch_host(self.plan, xh, xd, xb, yh, yd, yb, _stream(stream)),
+               "q4k_gemv_seq_launch_host")
+
 
 def q4k_gemv_seq(jobs, batch: int, layout: int = BLOCK144, workspace=None, stream=None):
     """One call of ``q4k_gemv_seq`` (plan and launch in one) over an ordered

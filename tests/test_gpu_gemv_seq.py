@@ -295,6 +295,13 @@ def test_host_buffer_step_matches_device_launch():
             assert torch.equal(got, y2[n].cpu()), f"step {step} {n}: bits differ from the device launch"
             y_ref, norm = O.gemv(slice_rows(fields[n], rows), x_np[SHAPES[n][2]])
             assert_close(got.numpy()[:, rows], y_ref, norm, f"step {step} {n}")
+    # the same step through buffers bound once (bind_host, step)
+    first = y_host.clone()
+    y_host.fill_(float("nan"))
+    seq.bind_host(x_host, x_dev, y_host, y_dev)
+    seq.step()
+    torch.cuda.synchronize()
+    assert torch.equal(y_host, first), "bound step: bits differ"
     assert q4k.q4k_device_error() == 0
 
 
